@@ -1,0 +1,430 @@
+"""Benchmark of the renderer bank-attention hot path on one GB300.
+
+A step is one ff_render_attn call of the Wan2.1-1.3B 480p workload at steady
+state: RoPE of the chunk's Q/K, publish of (K, V) into the stage bank, gather
+of 2 anchor + 15 history + 3 own latent frames (31200 keys), and attention of
+4680 queries x 12 heads x d 128 over them.  Steps rotate over the 4 stage banks
+(and over layers when more steps are asked for), always at chunks with full
+history.  Inputs are seeded synthetic tensors (AR(1) unit-RMS Q/K, N(0,1) V)
+already resident in HBM; each call touches ~440 MB, more than L2, so no extra
+flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Renderer bank-attention TFLOP/s (% BF16 peak) and chunk-steps/s on 1 GB300"
+WORKLOAD = "wan13b_480p"   # 12 heads, d 128, 30x52 tokens/frame, chunk 3 frames, H 5, 2 anchors
+LAYERS_PER_CHUNK_STEP = 30  # Wan2.1-1.3B transformer blocks: a chunk-step runs every layer once
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if isinstance(v, (int, float)):
+                    out[k] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_numbers(T=1560, heads=12, d=128, nq_frames=3, key_frames=20):
+    nq, nk = nq_frames * T, key_frames * T
+    flops = 4.0 * nq * nk * d * heads
+    F = T * heads * d * 2
+    # publish/gather algorithmic bytes per steady call: read q,k,v (9F) + anchors (4F)
+    # + history K/V (30F); write Q_rot (3F) + slot K/V (6F) + context K/V (40F)
+    g1_bytes = 92.0 * F
+    return nq, nk, flops, g1_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+
+    from kv_cache_attention_ff_gb300 import build, ff, synth
+
+    world, rank, local = dist_setup()
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    T, H, D = 1560, 12, 128
+    nq, nk, flops, g1_bytes = workload_numbers()
+    steady_per_layer = 4 * (27 - 5)  # chunks 5..26 of each stage have full history
+    total_calls = args.warmup + args.steps
+    n_layers = max(1, math.ceil(total_calls / steady_per_layer))
+    bank = ff.Bank(n_layers=n_layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                   total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, device=local)
+    stream = torch.cuda.Stream(device=dev)
+    cfg_id = 2
+    # anchors of every layer (3 planner blocks of 3)
+    with torch.cuda.stream(stream):
+        ka = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.K, list(range(0, 81, 10)), T, H, D, "ar",
+                                 device=dev)
+        va = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.V, list(range(0, 81, 10)), T, H, D, "normal",
+                                 device=dev)
+        for layer in range(n_layers):
+            for b in range(3):
+                sl = slice(3 * b * T, 3 * (b + 1) * T)
+                bank.anchor_publish(layer, 30 * b, 3, ka[sl].contiguous(), va[sl].contiguous(), stream)
+    # pool of 4 input sets (q, k, v) per stage, AR(1) over consecutive frames
+    pool = []
+    for st in range(4):
+        qs = synth.DeviceARStream(cfg_id, 0, st, synth.Q, T, H, D, "ar", device=dev)
+        ks = synth.DeviceARStream(cfg_id, 0, st, synth.K, T, H, D, "ar", device=dev)
+        vs = synth.DeviceARStream(cfg_id, 0, st, synth.V, T, H, D, "normal", device=dev)
+        pool.append([(qs.frames(3), ks.frames(3), vs.frames(3)) for _ in range(4)])
+    out = torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+
+    # ramp-up chunks 0..4 of every (layer, stage): untimed
+    for layer in range(n_layers):
+        for st in range(4):
+            for i in range(5):
+                q, k, v = pool[st][i % 4]
+                bank.render_attn(layer, st, i, q, k, v, out, stream)
+    next_chunk = {(l, s): 5 for l in range(n_layers) for s in range(4)}
+    order = [(l, s) for l in range(n_layers) for s in range(4)]
+    seq = []
+    while len(seq) < total_calls:
+        for key in order:
+            if next_chunk[key] < 27 and len(seq) < total_calls:
+                seq.append((key[0], key[1], next_chunk[key]))
+                next_chunk[key] += 1
+    assert all(c >= 5 for _, _, c in seq)
+    kernels_per_call = bank.kernel_count(10)
+
+    def call(j):
+        layer, st, c = seq[j]
+        q, k, v = pool[st][j % 4]
+        rc = bank.render_attn_raw(layer, st, c, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"ff_render_attn failed with status {rc}")
+
+    for j in range(args.warmup):
+        call(j)
+    torch.cuda.synchronize()
+    bank.set_timing(True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for j in range(args.warmup, total_calls):
+        call(j)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    kt = bank.read_timing()
+    bank.set_timing(False)
+    assert bank.error_poll() == 0, "device-side wait timed out"
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = flops * args.steps * world / (ms_total * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    attn_ms = kt.attn_ms / max(kt.calls, 1)
+    pub_ms = kt.publish_ms / max(kt.calls, 1)
+    comb_ms = kt.combine_ms / max(kt.calls, 1)
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    pub_gbs = g1_bytes / (pub_ms * 1e-3) / 1e9
+    roofline = {"kernel": "bank_attn_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
+                "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "algorithmic_per_launch": f"{flops / 1e9:.1f} GFLOP (4*Nq*Nk*d*h)", "avg_launch_ms": round(attn_ms, 4)}
+    roofline_publish = {"kernel": "publish_gather_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
+                        "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                        "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (92 frames x 4.79 MB)",
+                        "avg_launch_ms": round(pub_ms, 4)}
+
+    # end to end: pinned host inputs -> device, call, output -> pinned host, every step
+    e2e = run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_budget)
+    bank.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded AR(1) unit-RMS Q/K, N(0,1) V)",
+            "config": {"workload": WORKLOAD, "heads": H, "head_dim": D, "tokens_per_frame": T, "queries": nq,
+                       "keys": nk, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (~440 MB touched per call)"},
+            "pct_bf16_peak": round(100 * value / peaks["bf16_tflops"], 2),
+            "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
+            "kernel_ms": {"publish_gather": round(pub_ms, 4), "attention": round(attn_ms, 4),
+                          "combine": round(comb_ms, 4)},
+            "roofline": roofline, "roofline_publish": roofline_publish,
+            "e2e": e2e, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
+    """Same calls through the public API with host buffers: H2D of q, k, v and D2H of
+    the output inside the timed region.  Uses fresh (layer) banks' later chunks."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff
+    T, H, D = 1560, 12, 128
+    nq = 3 * T
+    host_in = [[t.cpu().pin_memory() for t in pool[s][0]] for s in range(4)]
+    host_out = torch.empty((nq, H, D), dtype=torch.bfloat16).pin_memory()
+    dq = torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+    # a separate bank so the contract (sequential chunks) holds
+    steps = args.steps
+    warm = args.warmup
+    layers = max(1, math.ceil((steps + warm) / 88))
+    eb = ff.Bank(n_layers=layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                 total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, device=dev.index)
+    z = torch.zeros((9 * T, H, D), dtype=torch.bfloat16, device=dev)
+    for layer in range(layers):
+        for b in range(3):
+            eb.anchor_publish(layer, 30 * b, 3, z[: 3 * T], z[: 3 * T], stream)
+        for st in range(4):
+            for i in range(5):
+                q, k, v = pool[st][i % 4]
+                eb.render_attn(layer, st, i, q, k, v, out, stream)
+    nxt = {(l, s): 5 for l in range(layers) for s in range(4)}
+    order = [(l, s) for l in range(layers) for s in range(4)]
+    calls = []
+    while len(calls) < steps + warm:
+        for key in order:
+            if nxt[key] < 27 and len(calls) < steps + warm:
+                calls.append((key[0], key[1], nxt[key]))
+                nxt[key] += 1
+
+    def step(j):
+        layer, st, c = calls[j]
+        hq, hk, hv = host_in[st]
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+        rc = eb.render_attn_raw(layer, st, c, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), out.data_ptr(),
+                                stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"ff_render_attn failed with status {rc}")
+        with torch.cuda.stream(stream):
+            host_out.copy_(out, non_blocking=True)
+
+    for j in range(warm):
+        step(j)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for j in range(warm, warm + steps):
+        step(j)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    eb.close()
+    bytes_in = 3 * nq * H * D * 2
+    return {"value": round(flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_in,
+            "d2h_bytes_per_step": nq * H * D * 2, "ms_per_step": round(ms / steps, 4)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(rows: int, heads: int, seed: int = 0):
+    """Time the fp64 oracle's attention on `rows` query rows x `heads` heads of the
+    steady 1.3B call (31200 keys, d 128).  Returns (seconds, flops)."""
+    import numpy as np
+
+    from oracle import ff_oracle as fo
+    rng = np.random.default_rng(seed)
+    nk = 20 * 1560
+    q = rng.standard_normal((rows, heads, 128))
+    k = rng.standard_normal((nk, heads, 128))
+    v = rng.standard_normal((nk, heads, 128))
+    t0 = time.perf_counter()
+    fo.attention_f64(q, k, v)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * rows * nk * 128 * heads
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    # calibrate on a small sample, then size the timed sample to about budget_s
+    dt0, f0 = oracle_sample(128, 1)
+    rate = f0 / max(dt0, 1e-6)
+    rows = int(min(4680, max(128, budget_s * rate / (4.0 * 31200 * 128))))
+    dt, fl = oracle_sample(rows, 1, seed=1)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle attention of {rows} query rows x 1 head over the 31200 keys of the "
+                      f"steady 1.3B call ({fl / 1e9:.1f} GFLOP, {dt:.1f} s); rope/publish/gather not included"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    dt0, f0 = oracle_sample(64, 1)
+    rate = f0 / max(dt0, 1e-6)
+    # each step: a bounded sample sized so that all steps take about a minute
+    per_step_s = max(0.5, 60.0 / max(args.steps + args.warmup, 1))
+    rows = int(min(4680, max(16, per_step_s * rate / (4.0 * 31200 * 128))))
+    times, fl = [], 0.0
+    for j in range(args.warmup + args.steps):
+        dt, fl = oracle_sample(rows, 1, seed=j)
+        if j >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = fl * len(times) / total / 1e12
+    cores = _host_cores()
+    sample = (f"fp64 numpy oracle attention, {rows} query rows x 1 head x 31200 keys per step "
+              f"({fl / 1e9:.2f} GFLOP/step) of the steady 1.3B call")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / len(times), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "heads": 12, "head_dim": 128, "queries": 4680, "keys": 31200},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * ff.h -- C ABI of libff.so: the renderer bank-attention hot path of
+ * FlashForward on one GB300 (sm_103a).
+ *
+ * Source of the operation: "FlashForward가 디노이징 중 KV 캐시를 재사용해 자기회귀
+ * 영상 생성을 가속한다" (onedev.kr/papers/332), section "어떻게 동작하나" (how it
+ * works), Eq. (2):
+ *     (v_hat, K, V) = F_R(x, c, tau_k; A_Gamma(i), B_k^(i))
+ *     B_k^(i+1)    = Tail_H(B_k^(i) U (i, K, V))
+ * The renderer forward of chunk i at denoising stage k reads the clean-anchor
+ * KV chosen by Gamma(i) and the stage-matched KV of the last H chunks, and
+ * publishes its own in-flight K/V into the same stage bank; there is no
+ * cache-update-only forward.  Anchors: section "무엇과 다른가" (stride Delta,
+ * planner blocks of 3, cache-extraction forward per block).
+ *
+ * This library implements the attention part of F_R for one transformer
+ * layer per call: rotary position encoding of the chunk's Q/K, publish of
+ * (K, V) into the stage bank, gather of anchors + history + own K/V into a
+ * contiguous context, and softmax(Q K^T / sqrt(d)) V over that context.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are bf16, row-major [tokens, heads, head_dim] with tokens
+ *    frame-major and each latent frame row-major over (y, x).  Pointers are
+ *    DEVICE pointers of the bank's device unless stated otherwise, 16-byte
+ *    aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on it; inputs must stay valid and
+ *    outputs must not be read until the stream has passed the call.
+ *  - The caller owns all input/output buffers and streams; the bank owns all
+ *    memory it allocates.  No call allocates device memory after
+ *    ff_bank_create.
+ *  - Every call returns an ff_status.  On any error the bank state is left
+ *    unchanged and nothing is enqueued.  Nothing aborts the process.
+ *  - A bank may be used from one host thread at a time.
+ */
+#ifndef FF_H_
+#define FF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ff_status {
+  FF_OK = 0,
+  FF_ERR_ARG = 1,             /* null pointer, index out of range, unsupported shape */
+  FF_ERR_ORDER = 2,           /* chunk != next chunk of (layer, stage): calls are sequential */
+  FF_ERR_ANCHOR_MISSING = 3,  /* an anchor of Gamma(i) was never published or was evicted */
+  FF_ERR_OOM = 4,             /* device allocation failed or would exceed desc.max_bytes */
+  FF_ERR_CUDA = 5,            /* a CUDA runtime call failed */
+  FF_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up (reported by ff_bank_error_poll) */
+  FF_ERR_UNSUPPORTED = 7      /* device is not compute capability 10.3 */
+} ff_status;
+
+/* Bank description (plain old data).  Defaults from ff_desc_default follow
+ * the pages' experiment settings (onedev.kr/papers/332, "무엇과 다른가":
+ * B_R = 3, Delta = 10, S = 4, H = 5). */
+typedef struct ff_bank_desc {
+  int n_layers;         /* transformer layers, each with its own banks (>= 1) */
+  int n_stages;         /* S denoising stages = stage banks per layer (>= 1) */
+  int history;          /* H: chunks kept per stage bank (>= 1) */
+  int chunk_frames;     /* B_R: latent frames per renderer chunk (1..8) */
+  int anchor_stride;    /* Delta: latent frames between clean anchors (>= 1) */
+  int anchor_capacity;  /* slots of the per-layer anchor ring; anchor a -> slot (a/Delta) mod capacity */
+  int total_frames;     /* N latent frames of the video */
+  int heads;            /* attention heads h */
+  int head_dim;         /* d: 64 or 128 */
+  int frame_h;          /* latent frame height in tokens (rows, y) */
+  int frame_w;          /* latent frame width in tokens (columns, x); tokens per frame T = frame_h * frame_w */
+  double rope_theta;    /* rotary base theta (10000) */
+  size_t max_bytes;     /* 0 = unlimited; otherwise create fails with FF_ERR_OOM above this many device bytes */
+  int device;           /* CUDA device ordinal */
+} ff_bank_desc;
+
+typedef struct ff_bank ff_bank_t;
+
+/* Fill `d` with the defaults above (n_layers 1, N 81, 12 heads, d 128,
+ * 30 x 52 tokens, 9 anchor slots, device 0). */
+int ff_desc_default(ff_bank_desc* d);
+
+/* Allocate every device buffer the bank will ever use: the S x H stage
+ * slots and the anchor ring of every layer, per-stage context and Q
+ * scratch, the attention split scratch and the rotary tables.  Returns
+ * FF_ERR_ARG for an invalid description, FF_ERR_UNSUPPORTED if the device
+ * is not sm_103, FF_ERR_OOM if the total exceeds max_bytes or an allocation
+ * fails (nothing stays allocated then).  *out is set only on FF_OK. */
+int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out);
+
+/* Publish the clean anchor KV of `n_anchors` consecutive anchors
+ * first_anchor_frame, + Delta, ... (a planner block's cache-extraction
+ * forward; onedev.kr/papers/332, "무엇과 다른가").  k_pre, v: device bf16
+ * [n_anchors * T, heads, head_dim], anchor-major.  K is rotated at
+ * t = anchor frame and stored with V in slot (a / Delta) mod capacity of
+ * `layer`, replacing what that slot held.  Errors: FF_ERR_ARG if the first
+ * frame is not a multiple of Delta, the last anchor is past the video, or
+ * n_anchors is not in 1..anchor_capacity. */
+int ff_anchor_publish(ff_bank_t* bank, int layer, int first_anchor_frame, int n_anchors,
+                      const void* k_pre, const void* v, void* stream);
+
+/* Renderer bank attention of chunk `chunk` at stage `stage` of `layer`
+ * (Eq. (2) above).  q_pre, k_pre, v: device bf16 [F_i * T, heads, head_dim],
+ * F_i = frames of the chunk (B_R, or fewer for the last chunk), before
+ * rotary encoding.  out: device bf16 of the same shape,
+ * out = softmax(RoPE(Q) K_ctx^T / sqrt(d)) V_ctx per head, where the context
+ * is [Gamma(i) anchors; chunks max(0, i-H) .. i-1 of this stage; own chunk].
+ * Afterwards slot i mod H of (layer, stage) holds (i, RoPE(K), V).
+ * Errors: FF_ERR_ORDER unless chunk equals the next chunk of (layer, stage)
+ * (0, 1, 2, ... in order); FF_ERR_ANCHOR_MISSING if an anchor of Gamma(i) is
+ * not resident. */
+int ff_render_attn(ff_bank_t* bank, int layer, int stage, int chunk,
+                   const void* q_pre, const void* k_pre, const void* v, void* out, void* stream);
+
+/* Wait for all work the bank enqueued, then free everything.  NULL-safe. */
+int ff_bank_destroy(ff_bank_t* bank);
+
+/* ---- introspection (used by tests; host-side, no device work unless stated) ---- */
+
+/* Gamma(i): left anchor, right anchor (-1 if none) and their count. */
+int ff_bank_gamma(const ff_bank_t* bank, int chunk, int* left, int* right, int* n);
+
+/* Slot state.  stage >= 0: slot `slot` (0..H-1) of the stage bank; stage == -1:
+ * slot of the anchor ring.  chunk_tag = chunk index (stage bank) or anchor
+ * frame (anchor ring), -1 if empty; frames = latent frames held; k, v =
+ * device pointers to the slot's bf16 [frames * T, heads, head_dim] data
+ * (valid for the bank's lifetime; contents change with later calls). */
+int ff_bank_slot_info(const ff_bank_t* bank, int layer, int stage, int slot, int* chunk_tag,
+                      int* frames, const void** k, const void** v);
+
+/* Device bytes owned by the bank (constant from create to destroy). */
+int ff_bank_bytes(const ff_bank_t* bank, size_t* bytes);
+
+/* Synchronise the bank's device and read the device error word: FF_OK or
+ * FF_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel gave up; that call's
+ * output is undefined).  Clears the word. */
+int ff_bank_error_poll(ff_bank_t* bank);
+
+/* Static description of a status code. */
+const char* ff_status_string(int status);
+
+/* ---- host-only planning (no device needed) ---- */
+
+typedef struct ff_chunk_plan {
+  int first_frame;      /* first latent frame of the chunk */
+  int n_frames;         /* frames of the chunk */
+  int n_anchors;        /* 1 or 2 */
+  int anchors[2];       /* Gamma(i), left first */
+  int n_hist;           /* history chunks (min(i, H)) */
+  int hist_first;       /* oldest history chunk */
+  int hist_frames;      /* frames in the history chunks */
+  int slot;             /* stage-bank slot the chunk publishes into (i mod H) */
+  int key_frames;       /* anchors + history + own frames */
+} ff_chunk_plan;
+
+/* Chunk plan of `chunk` for a description (FF_ERR_ARG past the last chunk). */
+int ff_plan_chunk(const ff_bank_desc* desc, int chunk, ff_chunk_plan* out);
+
+/* ---- timing of the library's own kernels (CUDA events on the call's stream) ---- */
+
+typedef struct ff_kernel_times {
+  int calls;            /* ff_render_attn calls timed since the last reset */
+  double publish_ms;    /* summed duration of the RoPE + publish + gather kernel */
+  double attn_ms;       /* summed duration of the attention kernel */
+  double combine_ms;    /* summed duration of the split-combine kernel (0 when unsplit) */
+} ff_kernel_times;
+
+/* enable != 0: record events around each kernel of subsequent render calls.
+ * Resets the accumulated times. */
+int ff_bank_set_timing(ff_bank_t* bank, int enable);
+
+/* Synchronise on the recorded events and return the accumulated times. */
+int ff_bank_read_timing(ff_bank_t* bank, ff_kernel_times* out);
+
+/* Number of kernels one ff_render_attn call of `chunk` launches (2 or 3). */
+int ff_render_kernel_count(const ff_bank_t* bank, int chunk, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* FF_H_ */

@@ -1,0 +1,444 @@
+// Renderer bank attention on tcgen05 tensor cores.
+//
+// O = softmax(Q K^T / sqrt(d)) V per head over the gathered context
+// [Gamma(i) anchors; last H stage-matched chunks; own chunk] (FlashForward,
+// onedev.kr/papers/332, "어떻게 동작하나", Eq. (2); no mask inside the key set).
+// bf16 operands, fp32 accumulation in tensor memory, fp32 online softmax.
+//
+// One CTA per SM, 10 warps:
+//   warps 0-3  softmax warpgroup 0: rows 0..127 of the current 256-row query block
+//   warps 4-7  softmax warpgroup 1: rows 128..255
+//   warp  8    TMA producer: Q tiles and a ring of K/V tiles
+//   warp  9    TMEM allocator and single-thread MMA issuer
+// Tensor memory (512 columns): S0 | S1 | O0 | O1 (S: 128 fp32 columns, O: d).
+// Per key tile j the MMA thread issues S0 = Q0 K_j^T, S1 = Q1 K_j^T, then
+// O0 += P0 V_{j-1}, O1 += P1 V_{j-1}: the tensor pipe works on one tile's
+// products while the other warpgroup turns its scores into probabilities.
+// P goes through shared memory (bf16, 128-byte swizzled, K-major); V is read
+// MN-major straight from its TMA tile.  The running max is only raised when
+// it grows by more than 2^8 (in exp2 units), so O is rescaled rarely; the
+// final normalisation uses the same stale max, which keeps the result exact
+// up to rounding.
+//
+// Work split: a (head, query block) unit covers n_kv key tiles; units are cut
+// into n_split key ranges ("pieces") so that pieces fill whole waves of SMs.
+// Pieces are ordered (head, split, query block) and taken round-robin by the
+// persistent CTAs, so concurrently running CTAs stream the same key tiles
+// (L2 reuse).  Split pieces write unnormalised partials that a small combine
+// kernel merges.
+#include <cuda_bf16.h>
+
+#include "ff_internal.h"
+#include "ff_ptx.cuh"
+
+namespace ff {
+
+template <int D>
+struct AttnCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int KB = D / 64;                 // 128-byte column blocks per row
+  static constexpr int BLK = 128 * 128;             // bytes of one [128 rows x 64 bf16] swizzled block
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int NST = (D == 128) ? 3 : 4;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NST * KV_BYTES;
+  static constexpr int N_BARS = 2 + 2 * NST + 10 + 1;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers, TMEM slot, abort flag; 1024 B alignment slack
+  static_assert(N_BARS * 8 + 8 <= 256, "barrier area");
+  static_assert(SMEM <= 232448, "shared memory");
+  static constexpr int TMEM_S = 0;     // S0 at 0, S1 at 128
+  static constexpr int TMEM_O = 256;   // O0 at 256, O1 at 256 + D
+};
+
+constexpr int kAttnThreads = 320;
+
+template <int D>
+__device__ __forceinline__ void piece_coords(const AttnParams& p, int piece, int& head, int& qb, int& kv0, int& kv1) {
+  const int per_head = p.n_split * p.n_qb;
+  head = piece / per_head;
+  const int rem = piece - head * per_head;
+  const int split = rem / p.n_qb;
+  qb = rem - split * p.n_qb;
+  kv0 = static_cast<int>((static_cast<long long>(split) * p.n_kv) / p.n_split);
+  kv1 = static_cast<int>((static_cast<long long>(split + 1) * p.n_kv) / p.n_split);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
+  using C = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sKV = smem + C::OFF_KV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = bars + 2 + C::NST;
+  uint64_t* s_full = bars + 2 + 2 * C::NST;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_full + 4;
+  uint64_t* o_done = s_full + 6;
+  uint64_t* o_free = s_full + 8;
+  uint64_t* fin = s_full + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(s_free + t, 128);
+      mbar_init(p_full + t, 128);
+      mbar_init(o_done + t, 1);
+      mbar_init(o_free + t, 128);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint32_t* err = p.err;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      uint32_t n_load = 0;
+      int seg = 0;
+      bool ok = true;
+      for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x, ++seg) {
+        int head, qb, kv0, kv1;
+        piece_coords<D>(p, piece, head, qb, kv0, kv1);
+        if (seg > 0 && !(ok = mbar_wait(q_empty, (seg - 1) & 1, abort_flag, err))) break;
+        mbar_expect_tx(q_full, 2 * C::Q_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(sQ + t * C::Q_BYTES + kb * C::BLK, &tmQ, head * D + kb * 64, qb * 256 + t * 128, q_full);
+        const int n = kv1 - kv0;
+        // consumption order: K_0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}
+        for (int step = 0; step <= n && ok; ++step) {
+          for (int which = 0; which < 2; ++which) {
+            const bool is_k = (which == 0);
+            const int j = is_k ? step : step - 1;
+            if (is_k && step == n) continue;
+            if (!is_k && step == 0) continue;
+            const int stage = static_cast<int>(n_load % C::NST);
+            const uint32_t use = n_load / C::NST;
+            if (use > 0 && !(ok = mbar_wait(kv_empty + stage, (use - 1) & 1, abort_flag, err))) break;
+            mbar_expect_tx(kv_full + stage, C::KV_BYTES);
+            const CUtensorMap* map = is_k ? &tmK : &tmV;
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(sKV + stage * C::KV_BYTES + kb * C::BLK, map, head * D + kb * 64, (kv0 + j) * 128,
+                          kv_full + stage);
+            ++n_load;
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
+      constexpr uint32_t kIdescO = idesc_bf16(128, D, 1);
+      const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP), sKVa = smem_u32(sKV);
+      uint32_t n_kvc = 0, n_s[2] = {0, 0}, n_pv[2] = {0, 0};
+      int seg = 0;
+      bool ok = true;
+
+      auto pv = [&](int jj, int head_seg) -> bool {
+        const int stage = static_cast<int>(n_kvc % C::NST);
+        if (!mbar_wait(kv_full + stage, (n_kvc / C::NST) & 1, abort_flag, err)) return false;
+        tc_fence_after();
+        const uint32_t va = sKVa + stage * C::KV_BYTES;
+        for (int t = 0; t < 2; ++t) {
+          if (jj == 0 && head_seg > 0 && !mbar_wait(o_free + t, (head_seg - 1) & 1, abort_flag, err)) return false;
+          if (!mbar_wait(p_full + t, n_pv[t] & 1, abort_flag, err)) return false;
+          tc_fence_after();
+          const uint32_t pa = sPa + t * C::P_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc(pa + (kk >> 2) * C::BLK + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(va + kk * 2048, C::BLK, 1024);
+            mma_bf16_ss(tmem + C::TMEM_O + t * D, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(o_done + t);
+          ++n_pv[t];
+        }
+        mma_commit(kv_empty + stage);
+        ++n_kvc;
+        return true;
+      };
+
+      for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x, ++seg) {
+        int head, qb, kv0, kv1;
+        piece_coords<D>(p, piece, head, qb, kv0, kv1);
+        const int n = kv1 - kv0;
+        if (!(ok = mbar_wait(q_full, seg & 1, abort_flag, err))) break;
+        tc_fence_after();
+        for (int j = 0; j < n && ok; ++j) {
+          const int stage = static_cast<int>(n_kvc % C::NST);
+          if (!(ok = mbar_wait(kv_full + stage, (n_kvc / C::NST) & 1, abort_flag, err))) break;
+          tc_fence_after();
+          const uint32_t ka = sKVa + stage * C::KV_BYTES;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (n_s[t] > 0 && !(ok = mbar_wait(s_free + t, (n_s[t] - 1) & 1, abort_flag, err))) break;
+            tc_fence_after();
+            const uint32_t qa = sQa + t * C::Q_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+              mma_bf16_ss(tmem + C::TMEM_S + t * 128, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024),
+                          kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full + t);
+            ++n_s[t];
+          }
+          if (!ok) break;
+          mma_commit(kv_empty + stage);
+          ++n_kvc;
+          if (j == n - 1) mma_commit(q_empty);
+          if (j >= 1) ok = pv(j - 1, seg);
+        }
+        if (ok) ok = pv(n - 1, seg);
+      }
+      mma_commit(fin);
+      mbar_wait(fin, 0, abort_flag, err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TMEM_S + t * 128;
+    const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
+    const uint32_t p_row = smem_u32(sP + t * C::P_BYTES) + (r >> 3) * 1024 + (r & 7) * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t n_sf = 0, n_od = 0;
+    bool ok = true;
+    for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x) {
+      int head, qb, kv0, kv1;
+      piece_coords<D>(p, piece, head, qb, kv0, kv1);
+      const int n = kv1 - kv0;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = mbar_wait(s_full + t, n_sf & 1, abort_flag, err))) break;
+        ++n_sf;
+        tc_fence_after();
+        float s[128];
+        tmem_ld32(tS + 0, s);
+        tmem_ld32(tS + 32, s + 32);
+        tmem_ld32(tS + 64, s + 64);
+        tmem_ld32(tS + 96, s + 96);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free + t);
+        const int tile = kv0 + j;
+        if (tile == p.n_kv - 1) {
+          const int valid = p.nk - tile * 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= valid) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = mx * sl2;
+        const bool need = m_new > m_run + 8.0f;
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
+        }
+        uint32_t pk[64];
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = ex2_approx(__fmaf_rn(s[c], sl2, -m_run));
+          const float p1 = ex2_approx(__fmaf_rn(s[c + 1], sl2, -m_run));
+          sum += p0 + p1;
+          pk[c >> 1] = pack_bf16x2(p0, p1);
+        }
+        l_run = __fmaf_rn(l_run, alpha, sum);
+        if (j > 0) {
+          if (!(ok = mbar_wait(o_done + t, n_od & 1, abort_flag, err))) break;
+          ++n_od;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+              float o[32];
+              tmem_ld32(tO + cc, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tmem_st32(tO + cc, o);
+            }
+            tmem_wait_st();
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t addr = p_row + (c >> 3) * C::BLK + (((c & 7) ^ (r & 7)) << 4);
+          st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full + t);
+      }
+      if (!ok) break;
+      // epilogue: wait for the last P V product
+      if (!(ok = mbar_wait(o_done + t, n_od & 1, abort_flag, err))) break;
+      ++n_od;
+      tc_fence_after();
+      const int row = qb * 256 + t * 128 + r;
+      if (p.n_split == 1) {
+        const float inv = 1.0f / l_run;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(row) * p.heads + head) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          float o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_wait_ld();
+          if (row < p.nq) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                 pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                 pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                 pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+          }
+        }
+      } else {
+        const size_t prow = static_cast<size_t>(piece) * 256 + t * 128 + r;
+        float* dst = p.part_o + prow * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          float o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_wait_ld();
+          float4* d4 = reinterpret_cast<float4*>(dst + cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+        reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_run, l_run);
+      }
+      tc_fence_before();
+      mbar_arrive(o_free + t);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the key-range pieces of each (head, query block): with per-piece
+// running max m_s (log2 units), sum l_s and unnormalised O_s,
+//   m = max m_s,  l = sum l_s 2^(m_s - m),  O = sum O_s 2^(m_s - m) / l.
+template <int D>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int PER = D / 8;  // elements per thread
+  const int unit = blockIdx.x;  // head * n_qb + qb
+  const int head = unit / p.n_qb;
+  const int qb = unit - head * p.n_qb;
+  const int rloc = blockIdx.y * 32 + (threadIdx.x >> 3);  // 0..255
+  const int part = threadIdx.x & 7;
+  const int row = qb * 256 + rloc;
+  if (row >= p.nq) return;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float m = -INFINITY;
+  for (int s = 0; s < p.n_split; ++s) {
+    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + qb;
+    m = fmaxf(m, ml[piece * 256 + rloc].x);
+  }
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float l = 0.f;
+  for (int s = 0; s < p.n_split; ++s) {
+    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + qb;
+    const float2 v = ml[piece * 256 + rloc];
+    const float w = exp2f(v.x - m);
+    l = __fmaf_rn(v.y, w, l);
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (piece * 256 + rloc) * D + part * PER);
+#pragma unroll
+    for (int i = 0; i < PER / 4; ++i) {
+      const float4 o = src[i];
+      acc[4 * i] = __fmaf_rn(o.x, w, acc[4 * i]);
+      acc[4 * i + 1] = __fmaf_rn(o.y, w, acc[4 * i + 1]);
+      acc[4 * i + 2] = __fmaf_rn(o.z, w, acc[4 * i + 2]);
+      acc[4 * i + 3] = __fmaf_rn(o.w, w, acc[4 * i + 3]);
+    }
+  }
+  const float inv = 1.0f / l;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(row) * p.heads + head) * D + part * PER;
+  uint32_t w[PER / 2];
+#pragma unroll
+  for (int i = 0; i < PER / 2; ++i) w[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+#pragma unroll
+  for (int i = 0; i < PER / 8; ++i)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+size_t attention_smem_bytes(int head_dim) {
+  return head_dim == 128 ? AttnCfg<128>::SMEM : AttnCfg<64>::SMEM;
+}
+
+cudaError_t attention_configure(int head_dim) {
+  if (head_dim == 128)
+    return cudaFuncSetAttribute(bank_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                AttnCfg<128>::SMEM);
+  return cudaFuncSetAttribute(bank_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64>::SMEM);
+}
+
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnParams& p, int grid, cudaStream_t s) {
+  if (head_dim == 128)
+    bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, tk, tv, p);
+  else
+    bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
+  dim3 grid(p.heads * p.n_qb, 8);
+  if (head_dim == 128)
+    attn_combine_kernel<128><<<grid, 256, 0, s>>>(p);
+  else
+    attn_combine_kernel<64><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ff

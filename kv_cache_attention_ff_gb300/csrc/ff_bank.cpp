@@ -1,0 +1,757 @@
+// Host side of libff: the bank state machine behind the C ABI in ff.h.
+//
+// State contract (FlashForward, onedev.kr/papers/332, "어떻게 동작하나", Eq. (2)):
+// stage bank B_k of each layer is a ring of H chunk slots; chunk i reads
+// B_k^(i) = chunks max(0, i-H) .. i-1 and leaves B_k^(i+1) = Tail_H(B_k^(i) U (i, K, V))
+// by writing slot i mod H.  Clean anchors (section "무엇과 다른가", stride Delta)
+// live in a per-layer ring of anchor slots, anchor a in slot (a / Delta) mod cap.
+// Gamma(i): nearest anchor at or before the chunk's first frame and nearest at
+// or after its last frame (dropped past the end; used once if both coincide).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "ff.h"
+#include "ff_internal.h"
+
+using namespace ff;
+
+namespace {
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FF_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+#define FF_LOG(...)                          \
+  do {                                       \
+    if (log_enabled()) {                     \
+      std::fprintf(stderr, "[libff] " __VA_ARGS__); \
+      std::fputc('\n', stderr);              \
+    }                                        \
+  } while (0)
+
+struct SlotState {
+  int tag = -1;
+  int frames = 0;
+};
+
+struct TimedCall {
+  cudaEvent_t ev[4];
+  bool combine;
+};
+
+constexpr int kQBlock = 256;  // query rows per attention work unit
+constexpr int kKTile = 128;   // keys per attention tile
+
+}  // namespace
+
+struct ff_bank {
+  ff_bank_desc d{};
+  int sm_count = 0;
+  size_t frame_elems = 0;   // T * h * d
+  size_t frame_bytes = 0;
+  int max_key_frames = 0;
+  int max_pieces = 0;
+  size_t total_bytes = 0;
+  std::vector<void*> allocations;
+
+  // device memory
+  uint8_t* stage_kv = nullptr;   // [L][S][H][2][B_R frames]
+  uint8_t* anchor_kv = nullptr;  // [L][cap][2][1 frame]
+  struct Scratch {
+    uint8_t* ctx_k = nullptr;
+    uint8_t* ctx_v = nullptr;
+    uint8_t* q_rot = nullptr;
+    float* part_o = nullptr;
+    float* part_ml = nullptr;
+  };
+  std::vector<Scratch> scratch;  // per stage
+  double2* rope64 = nullptr;
+  float2* rope32 = nullptr;
+  int rope_y_base = 0, rope_x_base = 0, pt = 0, py = 0, px = 0;
+  unsigned int* err = nullptr;
+
+  // host state
+  std::vector<SlotState> stage_slots;   // [L][S][H]
+  std::vector<SlotState> anchor_slots;  // [L][cap]
+  std::vector<int> next_chunk;          // [L][S]
+
+  // cross-stream ordering
+  std::vector<cudaEvent_t> ev_stage;       // [S] after the latest render of stage k
+  std::vector<cudaStream_t> stage_stream;  // [S]
+  std::vector<bool> stage_used;
+  std::vector<cudaEvent_t> ev_anchor;      // [cap] after the latest publish touching the slot
+  std::vector<cudaStream_t> anchor_stream;
+  std::vector<bool> anchor_used;
+
+  // timing
+  bool timing = false;
+  std::vector<TimedCall> timed;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+
+  SlotState& sslot(int l, int s, int h) { return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * d.history + h]; }
+  const SlotState& sslot(int l, int s, int h) const {
+    return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * d.history + h];
+  }
+  SlotState& aslot(int l, int a) { return anchor_slots[static_cast<size_t>(l) * d.anchor_capacity + a]; }
+  const SlotState& aslot(int l, int a) const { return anchor_slots[static_cast<size_t>(l) * d.anchor_capacity + a]; }
+
+  size_t slot_bytes() const { return static_cast<size_t>(d.chunk_frames) * frame_bytes; }
+  uint8_t* stage_k(int l, int s, int h) const {
+    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * d.history + h) * 2 + 0) * slot_bytes();
+  }
+  uint8_t* stage_v(int l, int s, int h) const {
+    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * d.history + h) * 2 + 1) * slot_bytes();
+  }
+  uint8_t* anchor_k(int l, int a) const {
+    return anchor_kv + ((static_cast<size_t>(l) * d.anchor_capacity + a) * 2 + 0) * frame_bytes;
+  }
+  uint8_t* anchor_v(int l, int a) const {
+    return anchor_kv + ((static_cast<size_t>(l) * d.anchor_capacity + a) * 2 + 1) * frame_bytes;
+  }
+};
+
+namespace {
+
+int n_chunks(const ff_bank_desc& d) { return (d.total_frames + d.chunk_frames - 1) / d.chunk_frames; }
+
+int validate_desc(const ff_bank_desc* d) {
+  if (!d) return FF_ERR_ARG;
+  if (d->n_layers < 1 || d->n_stages < 1 || d->history < 1 || d->chunk_frames < 1 || d->chunk_frames > 8 ||
+      d->anchor_stride < 1 || d->anchor_capacity < 1 || d->total_frames < 1 || d->heads < 1 ||
+      (d->head_dim != 64 && d->head_dim != 128) || d->frame_h < 1 || d->frame_w < 1 || !(d->rope_theta > 0.0) ||
+      d->device < 0)
+    return FF_ERR_ARG;
+  if (2 + (d->history + 1) * d->chunk_frames > kMaxItems) return FF_ERR_ARG;
+  const long long T = static_cast<long long>(d->frame_h) * d->frame_w;
+  const long long upf = T * d->heads * d->head_dim / 8;
+  // every count the kernels index with 32-bit ints must fit
+  if (upf * (2 + (d->history + 1) * d->chunk_frames) > (1ll << 31) - 1) return FF_ERR_ARG;
+  if (T * (2 + (d->history + 1) * d->chunk_frames) > (1ll << 30)) return FF_ERR_ARG;
+  if (static_cast<long long>(d->heads) * d->head_dim * 2 % 16 != 0) return FF_ERR_ARG;
+  return FF_OK;
+}
+
+void plan(const ff_bank_desc& d, int i, ff_chunk_plan* p) {
+  const int s = d.chunk_frames * i;
+  const int e = std::min(s + d.chunk_frames - 1, d.total_frames - 1);
+  p->first_frame = s;
+  p->n_frames = e - s + 1;
+  const int left = d.anchor_stride * (s / d.anchor_stride);
+  const int right = d.anchor_stride * ((e + d.anchor_stride - 1) / d.anchor_stride);
+  p->anchors[0] = left;
+  p->anchors[1] = -1;
+  p->n_anchors = 1;
+  if (right != left && right <= d.total_frames - 1) {
+    p->anchors[1] = right;
+    p->n_anchors = 2;
+  }
+  p->hist_first = std::max(0, i - d.history);
+  p->n_hist = i - p->hist_first;
+  int hf = 0;
+  for (int j = p->hist_first; j < i; ++j) {
+    const int js = d.chunk_frames * j;
+    hf += std::min(js + d.chunk_frames - 1, d.total_frames - 1) - js + 1;
+  }
+  p->hist_frames = hf;
+  p->slot = i % d.history;
+  p->key_frames = p->n_anchors + hf + p->n_frames;
+}
+
+// Key-range splits per (head, query block) so that pieces fill the SMs:
+// minimise waves * (tiles per piece + per-piece overhead) + combine cost.
+int choose_split(int units, int n_kv, int sms) {
+  double best = 1e300;
+  int best_s = 1;
+  for (int s = 1; s <= std::min(4, n_kv); ++s) {
+    const long long pieces = static_cast<long long>(units) * s;
+    const long long waves = (pieces + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0) + (s > 1 ? 4.0 : 0.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_err(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FF_OK;
+  FF_LOG("%s: %s", what, cudaGetErrorString(e));
+  return FF_ERR_CUDA;
+}
+
+// 2-D tensor map over a bf16 [rows, heads * head_dim] buffer, 64 x 128 boxes, 128-byte swizzle.
+int make_map(const ff_bank* b, CUtensorMap* map, const void* base, int rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(b->d.heads) * b->d.head_dim, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(b->d.heads) * b->d.head_dim * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = b->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    FF_LOG("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return FF_ERR_CUDA;
+  }
+  return FF_OK;
+}
+
+void free_all(ff_bank* b) {
+  for (void* p : b->allocations) cudaFree(p);
+  b->allocations.clear();
+  for (cudaEvent_t e : b->ev_stage)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : b->ev_anchor)
+    if (e) cudaEventDestroy(e);
+  for (auto& tc : b->timed)
+    for (cudaEvent_t e : tc.ev) cudaEventDestroy(e);
+  b->ev_stage.clear();
+  b->ev_anchor.clear();
+  b->timed.clear();
+}
+
+int alloc(ff_bank* b, size_t bytes, void** out) {
+  if (bytes == 0) bytes = 16;
+  void* p = nullptr;
+  const cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    FF_LOG("cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    return FF_ERR_OOM;
+  }
+  b->allocations.push_back(p);
+  *out = p;
+  return FF_OK;
+}
+
+// Make `s` wait for the last render of every stage that ran on another stream.
+void wait_stage_events(ff_bank* b, cudaStream_t s, int only_stage) {
+  for (int k = 0; k < b->d.n_stages; ++k) {
+    if (only_stage >= 0 && k != only_stage) continue;
+    if (b->stage_used[k] && b->stage_stream[k] != s) cudaStreamWaitEvent(s, b->ev_stage[k], 0);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int ff_desc_default(ff_bank_desc* d) {
+  if (!d) return FF_ERR_ARG;
+  std::memset(d, 0, sizeof(*d));
+  d->n_layers = 1;
+  d->n_stages = 4;
+  d->history = 5;
+  d->chunk_frames = 3;
+  d->anchor_stride = 10;
+  d->anchor_capacity = 9;
+  d->total_frames = 81;
+  d->heads = 12;
+  d->head_dim = 128;
+  d->frame_h = 30;
+  d->frame_w = 52;
+  d->rope_theta = 10000.0;
+  d->max_bytes = 0;
+  d->device = 0;
+  return FF_OK;
+}
+
+const char* ff_status_string(int s) {
+  switch (s) {
+    case FF_OK: return "ok";
+    case FF_ERR_ARG: return "invalid argument";
+    case FF_ERR_ORDER: return "chunk out of order for this (layer, stage)";
+    case FF_ERR_ANCHOR_MISSING: return "anchor of Gamma(i) not resident";
+    case FF_ERR_OOM: return "out of device memory (or over max_bytes)";
+    case FF_ERR_CUDA: return "CUDA runtime error";
+    case FF_ERR_DEVICE_TIMEOUT: return "bounded device wait timed out";
+    case FF_ERR_UNSUPPORTED: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int ff_plan_chunk(const ff_bank_desc* d, int chunk, ff_chunk_plan* out) {
+  if (validate_desc(d) != FF_OK || !out || chunk < 0 || chunk >= n_chunks(*d)) return FF_ERR_ARG;
+  plan(*d, chunk, out);
+  return FF_OK;
+}
+
+int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
+  if (!out) return FF_ERR_ARG;
+  const int v = validate_desc(desc);
+  if (v != FF_OK) return v;
+  const ff_bank_desc& d = *desc;
+
+  int dev_count = 0;
+  if (cudaGetDeviceCount(&dev_count) != cudaSuccess || d.device >= dev_count) {
+    cudaGetLastError();
+    return FF_ERR_CUDA;
+  }
+  cudaDeviceProp prop{};
+  if (cudaGetDeviceProperties(&prop, d.device) != cudaSuccess) return FF_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return FF_ERR_UNSUPPORTED;
+  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
+
+  ff_bank* b = new ff_bank();
+  b->d = d;
+  b->sm_count = prop.multiProcessorCount;
+  const size_t T = static_cast<size_t>(d.frame_h) * d.frame_w;
+  b->frame_elems = T * d.heads * d.head_dim;
+  b->frame_bytes = b->frame_elems * 2;
+  b->max_key_frames = 2 + (d.history + 1) * d.chunk_frames;
+
+  // attention split scratch: the largest piece count any call of this bank can use
+  int max_pieces = 0;
+  for (int f = 1; f <= d.chunk_frames; ++f) {
+    const int nq = static_cast<int>(f * T);
+    const int n_qb = (nq + kQBlock - 1) / kQBlock;
+    for (int kf = f; kf <= b->max_key_frames; ++kf) {
+      const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile);
+      const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
+      if (s > 1) max_pieces = std::max(max_pieces, d.heads * n_qb * s);
+    }
+  }
+  b->max_pieces = max_pieces;
+
+  const int pt = (d.head_dim - 4 * (d.head_dim / 6)) / 2;
+  const int py = (d.head_dim / 6);
+  const int px = (d.head_dim / 6);
+  b->pt = pt;
+  b->py = py;
+  b->px = px;
+  b->rope_y_base = d.total_frames * pt;
+  b->rope_x_base = b->rope_y_base + d.frame_h * py;
+  const size_t n_rope = static_cast<size_t>(b->rope_x_base) + static_cast<size_t>(d.frame_w) * px;
+
+  const size_t stage_bytes = static_cast<size_t>(d.n_layers) * d.n_stages * d.history * 2 * b->slot_bytes();
+  const size_t anchor_bytes = static_cast<size_t>(d.n_layers) * d.anchor_capacity * 2 * b->frame_bytes;
+  const size_t ctx_bytes = static_cast<size_t>(b->max_key_frames) * b->frame_bytes;
+  const size_t qrot_bytes = b->slot_bytes();
+  const size_t part_o_bytes = static_cast<size_t>(max_pieces) * kQBlock * d.head_dim * 4;
+  const size_t part_ml_bytes = static_cast<size_t>(max_pieces) * kQBlock * 8;
+  const size_t per_stage = 2 * ctx_bytes + qrot_bytes + part_o_bytes + part_ml_bytes;
+  const size_t rope_bytes = n_rope * (sizeof(double2) + sizeof(float2));
+  b->total_bytes = stage_bytes + anchor_bytes + d.n_stages * per_stage + rope_bytes + 256;
+  if (d.max_bytes && b->total_bytes > d.max_bytes) {
+    FF_LOG("bank needs %zu bytes > max_bytes %zu", b->total_bytes, d.max_bytes);
+    delete b;
+    return FF_ERR_OOM;
+  }
+
+  int rc = FF_OK;
+  void* p = nullptr;
+  if ((rc = alloc(b, stage_bytes, &p)) != FF_OK) goto fail;
+  b->stage_kv = static_cast<uint8_t*>(p);
+  if ((rc = alloc(b, anchor_bytes, &p)) != FF_OK) goto fail;
+  b->anchor_kv = static_cast<uint8_t*>(p);
+  b->scratch.resize(d.n_stages);
+  for (int k = 0; k < d.n_stages; ++k) {
+    if ((rc = alloc(b, ctx_bytes, &p)) != FF_OK) goto fail;
+    b->scratch[k].ctx_k = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, ctx_bytes, &p)) != FF_OK) goto fail;
+    b->scratch[k].ctx_v = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, qrot_bytes, &p)) != FF_OK) goto fail;
+    b->scratch[k].q_rot = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, part_o_bytes, &p)) != FF_OK) goto fail;
+    b->scratch[k].part_o = static_cast<float*>(p);
+    if ((rc = alloc(b, part_ml_bytes, &p)) != FF_OK) goto fail;
+    b->scratch[k].part_ml = static_cast<float*>(p);
+  }
+  if ((rc = alloc(b, n_rope * sizeof(double2), &p)) != FF_OK) goto fail;
+  b->rope64 = static_cast<double2*>(p);
+  if ((rc = alloc(b, n_rope * sizeof(float2), &p)) != FF_OK) goto fail;
+  b->rope32 = static_cast<float2*>(p);
+  if ((rc = alloc(b, 256, &p)) != FF_OK) goto fail;
+  b->err = static_cast<unsigned int*>(p);
+
+  {
+    // Rotary table: omega_j = theta^(-2j / d_axis), angle = position * omega_j (fp64), libm cos/sin.
+    std::vector<double2> h64(n_rope);
+    std::vector<float2> h32(n_rope);
+    auto fill = [&](size_t base, int n_pos, int pairs, int d_axis) {
+      for (int pos = 0; pos < n_pos; ++pos)
+        for (int j = 0; j < pairs; ++j) {
+          const double omega = std::pow(d.rope_theta, -static_cast<double>(2 * j) / static_cast<double>(d_axis));
+          const double ang = static_cast<double>(pos) * omega;
+          const double c = std::cos(ang), s = std::sin(ang);
+          h64[base + static_cast<size_t>(pos) * pairs + j] = make_double2(c, s);
+          h32[base + static_cast<size_t>(pos) * pairs + j] = make_float2(static_cast<float>(c), static_cast<float>(s));
+        }
+    };
+    fill(0, d.total_frames, pt, 2 * pt);
+    fill(b->rope_y_base, d.frame_h, py, 2 * py);
+    fill(b->rope_x_base, d.frame_w, px, 2 * px);
+    if (cudaMemcpy(b->rope64, h64.data(), n_rope * sizeof(double2), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(b->rope32, h32.data(), n_rope * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(b->err, 0, 256) != cudaSuccess) {
+      rc = FF_ERR_CUDA;
+      goto fail;
+    }
+  }
+  {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      rc = FF_ERR_CUDA;
+      goto fail;
+    }
+    b->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (attention_configure(d.head_dim) != cudaSuccess) {
+    rc = FF_ERR_CUDA;
+    goto fail;
+  }
+
+  b->stage_slots.assign(static_cast<size_t>(d.n_layers) * d.n_stages * d.history, SlotState{});
+  b->anchor_slots.assign(static_cast<size_t>(d.n_layers) * d.anchor_capacity, SlotState{});
+  b->next_chunk.assign(static_cast<size_t>(d.n_layers) * d.n_stages, 0);
+  b->ev_stage.assign(d.n_stages, nullptr);
+  b->stage_stream.assign(d.n_stages, nullptr);
+  b->stage_used.assign(d.n_stages, false);
+  b->ev_anchor.assign(d.anchor_capacity, nullptr);
+  b->anchor_stream.assign(d.anchor_capacity, nullptr);
+  b->anchor_used.assign(d.anchor_capacity, false);
+  for (auto& e : b->ev_stage)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      rc = FF_ERR_CUDA;
+      goto fail;
+    }
+  for (auto& e : b->ev_anchor)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      rc = FF_ERR_CUDA;
+      goto fail;
+    }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    rc = FF_ERR_CUDA;
+    goto fail;
+  }
+  FF_LOG("bank created: %zu bytes, %d SMs, max pieces %d", b->total_bytes, b->sm_count, max_pieces);
+  *out = b;
+  return FF_OK;
+
+fail:
+  free_all(b);
+  delete b;
+  return rc;
+}
+
+int ff_bank_destroy(ff_bank_t* b) {
+  if (!b) return FF_OK;
+  cudaSetDevice(b->d.device);
+  cudaDeviceSynchronize();
+  free_all(b);
+  delete b;
+  return FF_OK;
+}
+
+int ff_bank_gamma(const ff_bank_t* b, int chunk, int* left, int* right, int* n) {
+  if (!b || chunk < 0 || chunk >= n_chunks(b->d)) return FF_ERR_ARG;
+  ff_chunk_plan p;
+  plan(b->d, chunk, &p);
+  if (left) *left = p.anchors[0];
+  if (right) *right = p.anchors[1];
+  if (n) *n = p.n_anchors;
+  return FF_OK;
+}
+
+int ff_bank_slot_info(const ff_bank_t* b, int layer, int stage, int slot, int* chunk_tag, int* frames,
+                      const void** k, const void** v) {
+  if (!b || layer < 0 || layer >= b->d.n_layers || stage < -1 || stage >= b->d.n_stages) return FF_ERR_ARG;
+  if (stage == -1) {
+    if (slot < 0 || slot >= b->d.anchor_capacity) return FF_ERR_ARG;
+    const SlotState& s = b->aslot(layer, slot);
+    if (chunk_tag) *chunk_tag = s.tag;
+    if (frames) *frames = s.frames;
+    if (k) *k = b->anchor_k(layer, slot);
+    if (v) *v = b->anchor_v(layer, slot);
+    return FF_OK;
+  }
+  if (slot < 0 || slot >= b->d.history) return FF_ERR_ARG;
+  const SlotState& s = b->sslot(layer, stage, slot);
+  if (chunk_tag) *chunk_tag = s.tag;
+  if (frames) *frames = s.frames;
+  if (k) *k = b->stage_k(layer, stage, slot);
+  if (v) *v = b->stage_v(layer, stage, slot);
+  return FF_OK;
+}
+
+int ff_bank_bytes(const ff_bank_t* b, size_t* bytes) {
+  if (!b || !bytes) return FF_ERR_ARG;
+  *bytes = b->total_bytes;
+  return FF_OK;
+}
+
+int ff_bank_error_poll(ff_bank_t* b) {
+  if (!b) return FF_ERR_ARG;
+  cudaSetDevice(b->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return FF_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, b->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FF_ERR_CUDA;
+  if (word) {
+    cudaMemset(b->err, 0, sizeof(word));
+    return FF_ERR_DEVICE_TIMEOUT;
+  }
+  return FF_OK;
+}
+
+int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_pre, const void* v, void* stream) {
+  if (!b || layer < 0 || layer >= b->d.n_layers || n < 1 || n > b->d.anchor_capacity || first < 0 ||
+      first % b->d.anchor_stride != 0 || first + (n - 1) * b->d.anchor_stride > b->d.total_frames - 1 || !k_pre ||
+      !v || !aligned16(k_pre) || !aligned16(v))
+    return FF_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(b->d.device) != cudaSuccess) return FF_ERR_CUDA;
+  const ff_bank_desc& d = b->d;
+
+  G1Params prm{};
+  prm.q_in = nullptr;
+  prm.k_in = k_pre;
+  prm.v_in = v;
+  prm.rope64 = b->rope64;
+  prm.rope32 = b->rope32;
+  prm.y_base = b->rope_y_base;
+  prm.x_base = b->rope_x_base;
+  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
+  prm.units_per_row = d.heads * d.head_dim / 8;
+  prm.units_per_head = d.head_dim / 8;
+  prm.frame_w = d.frame_w;
+  prm.pt = b->pt;
+  prm.py = b->py;
+  prm.px = b->px;
+  prm.n_items = n;
+  for (int j = 0; j < n; ++j) {
+    const int a = first + j * d.anchor_stride;
+    const int sl = (a / d.anchor_stride) % d.anchor_capacity;
+    G1Item& it = prm.items[j];
+    it.kind = kItemAnchor;
+    it.k = b->anchor_k(layer, sl);
+    it.v = b->anchor_v(layer, sl);
+    it.ctx = -1;
+    it.r = j;
+    it.t = a;
+    it.old_ctx = -1;
+  }
+  // The slots may still be read by renders on other streams.
+  wait_stage_events(b, s, -1);
+  int rc = cuda_err(launch_publish(prm, 0, s), "anchor publish launch");
+  if (rc != FF_OK) return rc;
+  for (int j = 0; j < n; ++j) {
+    const int a = first + j * d.anchor_stride;
+    const int sl = (a / d.anchor_stride) % d.anchor_capacity;
+    cudaEventRecord(b->ev_anchor[sl], s);
+    b->anchor_stream[sl] = s;
+    b->anchor_used[sl] = true;
+    b->aslot(layer, sl).tag = a;
+    b->aslot(layer, sl).frames = 1;
+  }
+  return FF_OK;
+}
+
+int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_pre, const void* k_pre, const void* v,
+                   void* out, void* stream) {
+  if (!b || layer < 0 || layer >= b->d.n_layers || stage < 0 || stage >= b->d.n_stages || chunk < 0 ||
+      chunk >= n_chunks(b->d) || !q_pre || !k_pre || !v || !out || !aligned16(q_pre) || !aligned16(k_pre) ||
+      !aligned16(v) || !aligned16(out))
+    return FF_ERR_ARG;
+  const ff_bank_desc& d = b->d;
+  int& next = b->next_chunk[static_cast<size_t>(layer) * d.n_stages + stage];
+  if (chunk != next) return FF_ERR_ORDER;
+  ff_chunk_plan pl;
+  plan(d, chunk, &pl);
+  int aslots[2];
+  for (int j = 0; j < pl.n_anchors; ++j) {
+    aslots[j] = (pl.anchors[j] / d.anchor_stride) % d.anchor_capacity;
+    if (b->aslot(layer, aslots[j]).tag != pl.anchors[j]) return FF_ERR_ANCHOR_MISSING;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
+  ff_bank::Scratch& sc = b->scratch[stage];
+
+  // ---- work items: context = [anchors ; history oldest..newest ; own]
+  G1Params prm{};
+  prm.q_in = q_pre;
+  prm.k_in = k_pre;
+  prm.v_in = v;
+  prm.q_rot = sc.q_rot;
+  prm.ctx_k = sc.ctx_k;
+  prm.ctx_v = sc.ctx_v;
+  prm.rope64 = b->rope64;
+  prm.rope32 = b->rope32;
+  prm.y_base = b->rope_y_base;
+  prm.x_base = b->rope_x_base;
+  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
+  prm.units_per_row = d.heads * d.head_dim / 8;
+  prm.units_per_head = d.head_dim / 8;
+  prm.frame_w = d.frame_w;
+  prm.pt = b->pt;
+  prm.py = b->py;
+  prm.px = b->px;
+  int n_items = 0;
+  int ctx = 0;
+  for (int j = 0; j < pl.n_anchors; ++j) {
+    G1Item& it = prm.items[n_items++];
+    it.kind = kItemCopy;
+    it.k = b->anchor_k(layer, aslots[j]);
+    it.v = b->anchor_v(layer, aslots[j]);
+    it.ctx = ctx++;
+    it.r = it.t = 0;
+    it.old_ctx = -1;
+  }
+  // history; frames of the slot this chunk overwrites are saved by the own items
+  int old_ctx_first = -1, old_frames = 0;
+  for (int jc = pl.hist_first; jc < chunk; ++jc) {
+    const int hs = jc % d.history;
+    const SlotState& st = b->sslot(layer, stage, hs);
+    if (st.tag != jc) return FF_ERR_ARG;  // internal invariant (Tail_H) broken
+    const bool overwritten = (hs == pl.slot);
+    if (overwritten) {
+      old_ctx_first = ctx;
+      old_frames = st.frames;
+    }
+    for (int r = 0; r < st.frames; ++r) {
+      if (overwritten && r < pl.n_frames) {
+        ++ctx;  // written by own item r
+        continue;
+      }
+      G1Item& it = prm.items[n_items++];
+      it.kind = kItemCopy;
+      it.k = b->stage_k(layer, stage, hs) + static_cast<size_t>(r) * b->frame_bytes;
+      it.v = b->stage_v(layer, stage, hs) + static_cast<size_t>(r) * b->frame_bytes;
+      it.ctx = ctx++;
+      it.r = it.t = 0;
+      it.old_ctx = -1;
+    }
+  }
+  const int own_ctx = ctx;
+  for (int r = 0; r < pl.n_frames; ++r) {
+    G1Item& it = prm.items[n_items++];
+    it.kind = kItemOwn;
+    it.k = b->stage_k(layer, stage, pl.slot) + static_cast<size_t>(r) * b->frame_bytes;
+    it.v = b->stage_v(layer, stage, pl.slot) + static_cast<size_t>(r) * b->frame_bytes;
+    it.ctx = own_ctx + r;
+    it.r = r;
+    it.t = pl.first_frame + r;
+    it.old_ctx = (old_ctx_first >= 0 && r < old_frames) ? old_ctx_first + r : -1;
+  }
+  ctx += pl.n_frames;
+  prm.n_items = n_items;
+  if (ctx != pl.key_frames) return FF_ERR_ARG;
+
+  const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
+  const int nq = static_cast<int>(pl.n_frames * T);
+  const int nk = static_cast<int>(pl.key_frames * T);
+
+  AttnParams ap{};
+  ap.out = out;
+  ap.err = b->err;
+  ap.nq = nq;
+  ap.nk = nk;
+  ap.heads = d.heads;
+  ap.n_qb = (nq + kQBlock - 1) / kQBlock;
+  ap.n_kv = (nk + kKTile - 1) / kKTile;
+  ap.n_split = choose_split(d.heads * ap.n_qb, ap.n_kv, b->sm_count);
+  if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->max_pieces) ap.n_split = 1;
+  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
+  ap.part_o = sc.part_o;
+  ap.part_ml = sc.part_ml;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
+
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map(b, &tq, sc.q_rot, nq)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tk, sc.ctx_k, nk)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tv, sc.ctx_v, nk)) != FF_OK) return rc;
+
+  // ---- ordering against other streams
+  wait_stage_events(b, s, stage);
+  for (int j = 0; j < pl.n_anchors; ++j)
+    if (b->anchor_used[aslots[j]] && b->anchor_stream[aslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[aslots[j]], 0);
+
+  TimedCall tc{};
+  if (b->timing) {
+    for (auto& e : tc.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return FF_ERR_CUDA;
+    cudaEventRecord(tc.ev[0], s);
+  }
+  if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
+  if (b->timing) cudaEventRecord(tc.ev[1], s);
+  const int grid = std::min(ap.n_pieces, b->sm_count);
+  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "attention launch")) != FF_OK) return rc;
+  if (b->timing) cudaEventRecord(tc.ev[2], s);
+  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
+  if (b->timing) {
+    cudaEventRecord(tc.ev[3], s);
+    tc.combine = ap.n_split > 1;
+    b->timed.push_back(tc);
+  }
+  cudaEventRecord(b->ev_stage[stage], s);
+  b->stage_stream[stage] = s;
+  b->stage_used[stage] = true;
+
+  SlotState& own = b->sslot(layer, stage, pl.slot);
+  own.tag = chunk;
+  own.frames = pl.n_frames;
+  ++next;
+  return FF_OK;
+}
+
+int ff_render_kernel_count(const ff_bank_t* b, int chunk, int* count) {
+  if (!b || !count || chunk < 0 || chunk >= n_chunks(b->d)) return FF_ERR_ARG;
+  ff_chunk_plan pl;
+  plan(b->d, chunk, &pl);
+  const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
+  const int n_qb = static_cast<int>((pl.n_frames * T + kQBlock - 1) / kQBlock);
+  const int n_kv = static_cast<int>((pl.key_frames * T + kKTile - 1) / kKTile);
+  int s = choose_split(b->d.heads * n_qb, n_kv, b->sm_count);
+  if (static_cast<long long>(b->d.heads) * n_qb * s > b->max_pieces) s = 1;
+  *count = s > 1 ? 3 : 2;
+  return FF_OK;
+}
+
+int ff_bank_set_timing(ff_bank_t* b, int enable) {
+  if (!b) return FF_ERR_ARG;
+  cudaSetDevice(b->d.device);
+  cudaDeviceSynchronize();
+  for (auto& tc : b->timed)
+    for (cudaEvent_t e : tc.ev) cudaEventDestroy(e);
+  b->timed.clear();
+  b->timing = enable != 0;
+  return FF_OK;
+}
+
+int ff_bank_read_timing(ff_bank_t* b, ff_kernel_times* out) {
+  if (!b || !out) return FF_ERR_ARG;
+  std::memset(out, 0, sizeof(*out));
+  for (auto& tc : b->timed) {
+    if (cudaEventSynchronize(tc.ev[3]) != cudaSuccess) return FF_ERR_CUDA;
+    float a = 0, c = 0, e = 0;
+    cudaEventElapsedTime(&a, tc.ev[0], tc.ev[1]);
+    cudaEventElapsedTime(&c, tc.ev[1], tc.ev[2]);
+    cudaEventElapsedTime(&e, tc.ev[2], tc.ev[3]);
+    out->publish_ms += a;
+    out->attn_ms += c;
+    out->combine_ms += tc.combine ? e : 0.0;
+    ++out->calls;
+  }
+  return FF_OK;
+}
+
+}  // extern "C"

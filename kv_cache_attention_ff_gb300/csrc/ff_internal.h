@@ -1,0 +1,80 @@
+// Structures shared by the host side of libff (ff_bank.cpp) and its kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ff {
+
+// ------------------------------------------------------------------ G1 / G2
+// One launch of the RoPE + publish + gather kernel processes a list of
+// frame-sized work items.  Every item covers one latent frame of one
+// tensor pair (K and V), T * heads * head_dim bf16 each, split into 16-byte
+// units; a thread handles the same unit offset of whatever an item touches.
+
+enum ItemKind : int {
+  kItemCopy = 0,    // context frame <- (k, v) source frame (anchor or history slot)
+  kItemOwn = 1,     // own chunk frame r: RoPE(q) -> q_rot, RoPE(k) and v -> slot frame r and context
+  kItemAnchor = 2,  // anchor input frame r: RoPE(k) and v -> anchor slot
+};
+
+struct G1Item {
+  const void* k;   // copy: source K frame; own/anchor: destination K frame (slot)
+  const void* v;   // same for V
+  int kind;
+  int ctx;         // copy/own: context frame written (-1: none)
+  int r;           // own/anchor: frame index in the call's inputs
+  int t;           // own/anchor: absolute latent frame (rotary time position)
+  int old_ctx;     // own: context frame that receives the slot's previous content
+                   // before it is overwritten (-1: nothing to save)
+  int pad;
+};
+
+constexpr int kMaxItems = 160;
+
+struct G1Params {
+  const void* q_in;   // own chunk inputs [F * T, h, d] (q unused for anchors)
+  const void* k_in;
+  const void* v_in;
+  void* q_rot;        // [F * T, h, d]
+  void* ctx_k;        // [key_frames * T, h, d]
+  void* ctx_v;
+  const double2* rope64;  // rotary (cos, sin) in fp64: [total_frames][pt], then [frame_h][py], then [frame_w][px]
+  const float2* rope32;   // the same table rounded to fp32
+  int y_base, x_base;     // first row-axis and column-axis entries
+  long long units_per_frame;  // T * h * d / 8
+  int units_per_row;          // h * d / 8  (16-byte units per token)
+  int units_per_head;         // d / 8
+  int frame_w;
+  int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
+  int px;
+  int n_items;
+  G1Item items[kMaxItems];
+};
+
+// ----------------------------------------------------------------- attention
+
+struct AttnParams {
+  void* out;            // bf16 [Nq, h, d]
+  float* part_o;        // [pieces][256][d] unnormalised partial outputs (split only)
+  float* part_ml;       // [pieces][256][2] running max (log2 units) and sum
+  unsigned int* err;    // device error word
+  int nq, nk, heads;
+  int n_qb;             // 256-row query blocks
+  int n_kv;             // 128-key tiles
+  int n_split;          // key-range splits per query block
+  int n_pieces;         // heads * n_split * n_qb
+  float scale_log2;     // log2(e) / sqrt(d)
+};
+
+// Host launchers (ff_publish.cu / ff_attn.cu).
+cudaError_t launch_publish(const G1Params& p, int grid, cudaStream_t s);
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnParams& p, int grid, cudaStream_t s);
+cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s);
+size_t attention_smem_bytes(int head_dim);
+cudaError_t attention_configure(int head_dim);
+
+}  // namespace ff

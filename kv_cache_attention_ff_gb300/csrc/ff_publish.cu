@@ -1,0 +1,221 @@
+// RoPE + publish + gather kernel (and its anchor-publish form).
+//
+// FlashForward renderer forward (onedev.kr/papers/332, "어떻게 동작하나", Eq. (2)):
+// the chunk's own K/V are computed by the denoising forward and published into
+// the stage bank, B_k^(i+1) = Tail_H(B_k^(i) U (i, K, V)); the chunk attends over
+// Gamma(i) anchors, the last H stage-matched chunks and itself.  This kernel
+// does the memory side of one such call:
+//   * RoPE of the chunk's Q (fp32 arithmetic, bf16 out) into a scratch buffer;
+//   * RoPE of the chunk's K under the published-K contract (below) and the
+//     store of (K, V) into bank slot i mod H;
+//   * the gather of [anchors; history; own] K/V into one contiguous context.
+// The slot being overwritten still holds chunk i-H, which chunk i attends to:
+// the thread that writes unit u of the new chunk first reads unit u of the old
+// one and saves it into the context, so the read precedes the write in one
+// thread's program order (plain coherent loads for that slot).
+//
+// Published-K contract: each rotated pair is
+//   a' = RNE_bf16(fl64(fl64(a c) - fl64(b s))),  b' = RNE_bf16(fl64(fl64(a s) + fl64(b c)))
+// with c, s the fp64 cosine/sine.  fp64 is slow on this part, so every value is
+// first evaluated in fp32 with an error bound and accepted only when the whole
+// error interval rounds to one bf16 value (Ziv's rounding test: monotone
+// rounding of both interval ends agrees); otherwise the exact fp64 expression
+// is evaluated.  Either way the result is the contract's value.
+#include <cuda_bf16.h>
+
+#include "ff_internal.h"
+#include "ff_ptx.cuh"
+
+namespace ff {
+
+// fp64 -> bf16 with one round-to-nearest-even, from the binary64 bit fields.
+__device__ __forceinline__ uint32_t f64_to_bf16_rne(double v) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  const uint32_t sign = static_cast<uint32_t>(b >> 63) << 15;
+  const int ex = static_cast<int>((b >> 52) & 0x7FF);
+  const unsigned long long man = b & 0xFFFFFFFFFFFFFull;
+  if (ex == 0x7FF) return man ? (sign | 0x7FC0u) : (sign | 0x7F80u);
+  if (ex == 0) return sign;  // fp64 zero or subnormal: rounds to a signed zero
+  const int e = ex - 1023;
+  const unsigned long long sig = man | (1ull << 52);  // value = sig * 2^(e - 52)
+  if (e >= -126) {
+    unsigned long long keep = sig >> 45;  // 8 significant bits
+    const unsigned long long rem = sig & ((1ull << 45) - 1);
+    const unsigned long long half = 1ull << 44;
+    if (rem > half || (rem == half && (keep & 1ull))) ++keep;
+    int ee = e;
+    if (keep == 256ull) {
+      keep = 128ull;
+      ++ee;
+    }
+    if (ee > 127) return sign | 0x7F80u;
+    return sign | (static_cast<uint32_t>(ee + 127) << 7) | static_cast<uint32_t>(keep & 0x7Full);
+  }
+  // bf16 subnormal range: count units of 2^-133, value / 2^-133 = sig >> (-e - 81)
+  const int s = -e - 81;
+  if (s >= 54) return sign;
+  unsigned long long keep = sig >> s;
+  const unsigned long long rem = sig & ((1ull << s) - 1);
+  const unsigned long long half = 1ull << (s - 1);
+  if (rem > half || (rem == half && (keep & 1ull))) ++keep;
+  return sign | static_cast<uint32_t>(keep);  // keep == 128 is the smallest normal
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// One component of a rotated K pair: RNE_bf16(fl64(fl64(a u) -/+ fl64(b w))).
+// u32/w32 are the fp32 roundings of u/w; the fp64 values are fetched only when
+// the fast evaluation cannot decide the rounding.
+// cs points at the fp64 (cos, sin) pair; kSwap selects (u, w) = (sin, cos).
+template <bool kSub, bool kSwap>
+__device__ __forceinline__ uint32_t rot_k(float a, float b, float u32, float w32, const double* cs) {
+  const float p1 = __fmul_rn(a, u32);
+  const float p2 = __fmul_rn(b, w32);
+  const float r = kSub ? __fsub_rn(p1, p2) : __fadd_rn(p1, p2);
+  // |r - exact| <= ~1.5 * 2^-23 (|a u| + |b w|) + 3 * 2^-150; the margin below is 8x that.
+  const float mag = __fadd_rn(fabsf(p1), fabsf(p2));
+  const float err = __fmaf_rn(mag, 0x1p-19f, 0x1p-140f);
+  const uint32_t lo = bf16_bits(__fsub_rn(r, err));
+  const uint32_t hi = bf16_bits(__fadd_rn(r, err));
+  if (lo == hi && isfinite(r) && isfinite(mag)) return lo;
+  const double u = __ldg(cs + (kSwap ? 1 : 0));
+  const double w = __ldg(cs + (kSwap ? 0 : 1));
+  const double pa = __dmul_rn(static_cast<double>(a), u);
+  const double pb = __dmul_rn(static_cast<double>(b), w);
+  return f64_to_bf16_rne(kSub ? __dsub_rn(pa, pb) : __dadd_rn(pa, pb));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_coherent(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ void st_u4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Index of channel pair `pair` for a token at (t, y, x) in the rotary tables
+// (time rows, then row-axis rows, then column-axis rows).
+__device__ __forceinline__ int rope_index(const G1Params& p, int pair, int t, int y, int x) {
+  if (pair < p.pt) return t * p.pt + pair;
+  pair -= p.pt;
+  if (pair < p.py) return p.y_base + y * p.py + pair;
+  pair -= p.py;
+  return p.x_base + x * p.px + pair;
+}
+
+constexpr int kPubThreads = 256;
+constexpr int kPubUnroll = 2;
+
+__global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __grid_constant__ G1Params p) {
+  const G1Item& I = p.items[blockIdx.y];
+  const int upf = static_cast<int>(p.units_per_frame);
+  const int kind = I.kind;
+  const uint4* k_in = static_cast<const uint4*>(p.k_in);
+  const uint4* v_in = static_cast<const uint4*>(p.v_in);
+  const uint4* q_in = static_cast<const uint4*>(p.q_in);
+  uint4* ctx_k = static_cast<uint4*>(p.ctx_k);
+  uint4* ctx_v = static_cast<uint4*>(p.ctx_v);
+  uint4* slot_k = static_cast<uint4*>(const_cast<void*>(I.k));
+  uint4* slot_v = static_cast<uint4*>(const_cast<void*>(I.v));
+
+  const int base = blockIdx.x * (kPubThreads * kPubUnroll) + threadIdx.x;
+  if (kind == kItemCopy) {
+    uint4 kk[kPubUnroll], vv[kPubUnroll];
+#pragma unroll
+    for (int j = 0; j < kPubUnroll; ++j) {
+      const int off = base + j * kPubThreads;
+      if (off < upf) {
+        kk[j] = ld_stream(slot_k + off);
+        vv[j] = ld_stream(slot_v + off);
+      }
+    }
+    const size_t cbase = static_cast<size_t>(I.ctx) * upf;
+#pragma unroll
+    for (int j = 0; j < kPubUnroll; ++j) {
+      const int off = base + j * kPubThreads;
+      if (off < upf) {
+        st_u4(ctx_k + cbase + off, kk[j]);
+        st_u4(ctx_v + cbase + off, vv[j]);
+      }
+    }
+    return;
+  }
+
+  // Own-chunk frame or anchor frame.
+  const bool own = (kind == kItemOwn);
+  const bool save_old = own && I.old_ctx >= 0;
+  const size_t in_base = static_cast<size_t>(I.r) * upf;
+#pragma unroll
+  for (int j = 0; j < kPubUnroll; ++j) {
+    const int off = base + j * kPubThreads;
+    if (off >= upf) break;
+    const uint4 kin = ld_stream(k_in + in_base + off);
+    const uint4 vin = ld_stream(v_in + in_base + off);
+    uint4 qin = make_uint4(0, 0, 0, 0);
+    if (own) qin = ld_stream(q_in + in_base + off);
+    uint4 oldk = make_uint4(0, 0, 0, 0), oldv = make_uint4(0, 0, 0, 0);
+    if (save_old) {  // read the slot's previous chunk before this thread overwrites it
+      oldk = ld_coherent(slot_k + off);
+      oldv = ld_coherent(slot_v + off);
+    }
+    const int tok = off / p.units_per_row;
+    const int in_row = off - tok * p.units_per_row;
+    const int pair0 = (in_row % p.units_per_head) * 4;
+    const int ty = tok / p.frame_w;
+    const int tx = tok - ty * p.frame_w;
+    const uint32_t kw[4] = {kin.x, kin.y, kin.z, kin.w};
+    const uint32_t qw[4] = {qin.x, qin.y, qin.z, qin.w};
+    uint32_t ko[4], qo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = rope_index(p, pair0 + e, I.t, ty, tx);
+      const float2 cs = __ldg(p.rope32 + idx);
+      const double* cs64 = reinterpret_cast<const double*>(p.rope64 + idx);
+      const float a = bf_lo(kw[e]), b = bf_hi(kw[e]);
+      // a' = a c - b s ; b' = a s + b c
+      const uint32_t a2 = rot_k<true, false>(a, b, cs.x, cs.y, cs64);
+      const uint32_t b2 = rot_k<false, true>(a, b, cs.y, cs.x, cs64);
+      ko[e] = a2 | (b2 << 16);
+      const float qa = bf_lo(qw[e]), qb = bf_hi(qw[e]);
+      const float qa2 = __fmaf_rn(qa, cs.x, -__fmul_rn(qb, cs.y));
+      const float qb2 = __fmaf_rn(qa, cs.y, __fmul_rn(qb, cs.x));
+      qo[e] = bf16_bits(qa2) | (bf16_bits(qb2) << 16);
+    }
+    const uint4 kout = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    if (save_old) {
+      const size_t ob = static_cast<size_t>(I.old_ctx) * upf + off;
+      st_u4(ctx_k + ob, oldk);
+      st_u4(ctx_v + ob, oldv);
+    }
+    st_u4(slot_k + off, kout);
+    st_u4(slot_v + off, vin);
+    if (own) {
+      const size_t cb = static_cast<size_t>(I.ctx) * upf + off;
+      st_u4(ctx_k + cb, kout);
+      st_u4(ctx_v + cb, vin);
+      st_u4(static_cast<uint4*>(p.q_rot) + in_base + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
+    }
+  }
+}
+
+cudaError_t launch_publish(const G1Params& p, int /*grid_hint*/, cudaStream_t s) {
+  const int upf = static_cast<int>(p.units_per_frame);
+  dim3 grid((upf + kPubThreads * kPubUnroll - 1) / (kPubThreads * kPubUnroll), p.n_items);
+  publish_gather_kernel<<<grid, kPubThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ff

@@ -85,3 +85,73 @@ class ARStream:
         self.f += 1
         rms = np.sqrt(np.mean(self.z * self.z, axis=-1, keepdims=True, dtype=np.float32))
         return f32_to_bf16_bits(self.z / rms)
+
+
+# ---------------------------------------------------------------------------
+# Device-side generation (same recipe, torch's seeded CUDA generator) for the
+# large workloads.  Consumers that need host copies (the oracle) copy these
+# tensors back; the values never depend on the library under test.
+# ---------------------------------------------------------------------------
+
+def _seed(cfg_id, layer, stream, tensor, frame) -> int:
+    return int(np.random.SeedSequence([cfg_id, layer, stream, tensor, frame]).generate_state(1, np.uint64)[0] >> 1)
+
+
+def _bf16_torch(x):
+    import torch
+    u = x.contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.to(torch.int32).to(torch.int16).view(torch.bfloat16)
+
+
+class DeviceARStream:
+    """Consecutive frames of one (cfg, layer, stream, tensor) process on the GPU,
+    as bf16 tensors [tokens, heads, head_dim]; mode "ar" or "normal"."""
+
+    def __init__(self, cfg_id, layer, stream, tensor, tokens, heads, head_dim, mode, device="cuda"):
+        self.key = (cfg_id, layer, stream, tensor)
+        self.shape = (tokens, heads, head_dim)
+        self.mode = mode
+        self.device = device
+        self.f = 0
+        self.z = None
+
+    def _eps(self, f):
+        import torch
+        g = torch.Generator(device=self.device)
+        g.manual_seed(_seed(*self.key, f))
+        return torch.randn(self.shape, generator=g, device=self.device, dtype=torch.float32)
+
+    def next(self):
+        import torch
+        e = self._eps(self.f)
+        self.f += 1
+        if self.mode == "normal":
+            return _bf16_torch(e)
+        c = float(np.float32(np.sqrt(1.0 - RHO * RHO)))
+        self.z = e if self.z is None else self.z * RHO + e * c
+        rms = torch.sqrt(torch.mean(self.z * self.z, dim=-1, keepdim=True))
+        return _bf16_torch(self.z / rms)
+
+    def frames(self, n):
+        import torch
+        return torch.cat([self.next() for _ in range(n)], dim=0)
+
+
+def device_frames(cfg_id, layer, stream, tensor, frames, tokens, heads, head_dim, mode, device="cuda"):
+    """bf16 [len(frames) * tokens, heads, head_dim] on the device for the given
+    absolute frames (AR mode regenerates the prefix on the device)."""
+    import torch
+    s = DeviceARStream(cfg_id, layer, stream, tensor, tokens, heads, head_dim, mode, device)
+    want = {f: r for r, f in enumerate(frames)}
+    out = [None] * len(frames)
+    if mode == "normal":
+        for f, r in want.items():
+            s.f = f
+            out[r] = s.next()
+    else:
+        for f in range(max(frames) + 1):
+            x = s.next()
+            if f in want:
+                out[want[f]] = x
+    return torch.cat(out, dim=0)

@@ -1,0 +1,98 @@
+"""CPU-side checks of libff: it loads, exports every entry point that
+include/ff.h declares, and its host-only chunk planner agrees with the
+oracle's schedule."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import ff_oracle as fo
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ff():
+    from kv_cache_attention_ff_gb300 import build, ff as ffmod
+    build.build()
+    return ffmod
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ff.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(ff_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(ff):
+    names = _declared()
+    assert "ff_render_attn" in names and "ff_bank_create" in names
+    lib = ctypes.CDLL(ff.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(ff.EXPORTS) == names
+
+
+def test_status_strings(ff):
+    for code in range(8):
+        assert ff.lib().ff_status_string(code)
+    assert ff.lib().ff_status_string(2) == b"chunk out of order for this (layer, stage)"
+
+
+@pytest.mark.parametrize("fields", [
+    dict(total_frames=81, chunk_frames=3, anchor_stride=10, history=5),
+    dict(total_frames=13, chunk_frames=3, anchor_stride=4, history=2, anchor_capacity=4, heads=2, head_dim=64,
+         frame_h=4, frame_w=4),
+    dict(total_frames=261, chunk_frames=3, anchor_stride=10, history=5, anchor_capacity=6),
+    dict(total_frames=75, chunk_frames=3, anchor_stride=10, history=1),
+    dict(total_frames=50, chunk_frames=4, anchor_stride=7, history=3),
+])
+def test_plan_matches_oracle(ff, fields):
+    d = ff.make_desc(**fields)
+    N, B, S, H = fields["total_frames"], fields["chunk_frames"], fields["anchor_stride"], fields["history"]
+    for i in range(fo.num_chunks(N, B)):
+        p = ff.plan_chunk(d, i)
+        s, e = fo.chunk_span(i, B, N)
+        g = fo.gamma(i, B, S, N)
+        hist = fo.history_chunks(i, H)
+        assert (p.first_frame, p.n_frames) == (s, e - s + 1)
+        assert list(p.anchors)[:p.n_anchors] == g and p.n_anchors == len(g)
+        assert p.n_hist == len(hist) and (not hist or p.hist_first == hist[0])
+        hf = sum(fo.chunk_span(j, B, N)[1] - fo.chunk_span(j, B, N)[0] + 1 for j in hist)
+        assert p.hist_frames == hf
+        assert p.slot == fo.bank_slot(i, H)
+        assert p.key_frames == len(g) + hf + (e - s + 1)
+    with pytest.raises(ff.FFError) as ei:
+        ff.plan_chunk(d, fo.num_chunks(N, B))
+    assert ei.value.code == "FF_ERR_ARG"
+
+
+def test_invalid_descriptions_rejected_before_device(ff):
+    for bad in (dict(head_dim=96), dict(history=0), dict(chunk_frames=0), dict(heads=0), dict(rope_theta=0.0),
+                dict(history=60)):
+        d = ff.make_desc(**bad)
+        h = ctypes.c_void_p()
+        assert ff.lib().ff_bank_create(ctypes.byref(d), ctypes.byref(h)) == 1
+        assert not h.value
+
+
+def test_create_without_gpu_fails_cleanly(ff):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    d = ff.make_desc()
+    h = ctypes.c_void_p()
+    assert ff.lib().ff_bank_create(ctypes.byref(d), ctypes.byref(h)) in (5, 7)
+    assert not h.value
+    assert ff.lib().ff_bank_destroy(None) == 0
+
+
+def test_synth_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    from kv_cache_attention_ff_gb300 import synth
+    x = np.random.default_rng(0).standard_normal(100000).astype(np.float32) * 3
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(synth.f32_to_bf16_bits(x), ref)
+    got = synth._bf16_torch(torch.from_numpy(x)).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
