@@ -248,7 +248,7 @@ def run_gpu(args):
                         "avg_launch_ms": round(pub_ms, 4)}
 
     # end to end: pinned host inputs -> device, call, output -> pinned host, every step
-    e2e = run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
+    e2e = None if args.no_e2e else run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -417,6 +417,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
