@@ -175,6 +175,35 @@ int ff_bank_read_timing(ff_bank_t* bank, ff_kernel_times* out);
 /* Number of kernels one ff_render_attn call of `chunk` launches (2 or 3). */
 int ff_render_kernel_count(const ff_bank_t* bank, int chunk, int* count);
 
+/* ---- attention without any device allocation ----
+ *
+ * The pages have no counterpart of this entry point.  It serves callers that
+ * cannot call cudaMalloc: code running inside a CUDA stream capture, hosts
+ * whose memory is owned by another allocator, processes that must not grow
+ * their device footprint after start-up.  Such a caller holds the rotated
+ * queries and the gathered context itself and needs only the attention step.
+ *
+ * out = softmax(q k^T / sqrt(head_dim)) v per head, computed by the same
+ * tcgen05 kernel as ff_render_attn.  q, out: device bf16 [nq, heads, head_dim];
+ * k, v: device bf16 [nk, heads, head_dim]; all 16-byte aligned, owned by the
+ * caller; head_dim 64 or 128.  Asynchronous on `stream` (a cudaStream_t).
+ *
+ * Scratch: key-range split partials live in one static device array of
+ * FF_NOALLOC_SCRATCH_BYTES, created when the library's module loads on a
+ * device and kept until the process exits.  A call needs
+ * 256 + heads * ceil(nq/256) * n_split * 256 * (4 * head_dim + 8) bytes of it
+ * (n_split in 2..4 chosen by the library, 1 when nk <= 128); larger problems
+ * are rejected with FF_ERR_ARG before any work is enqueued.  The first call
+ * on a device (that device current) sets up the array's address and the
+ * kernel attributes: make it before any stream capture.  All calls share the
+ * array, so calls that overlap on the GPU race; order them on one stream.
+ * A bounded device wait that gives up leaves `out` undefined and is not
+ * reported by this entry point.  Returns FF_OK, FF_ERR_ARG, FF_ERR_CUDA or
+ * FF_ERR_UNSUPPORTED (device not sm_103). */
+#define FF_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int ff_attention_noalloc(const void* q, const void* k, const void* v, void* out, int nq, int nk, int heads,
+                         int head_dim, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,153 @@
+// ff_attention_noalloc: the attention kernel of libff for callers that cannot
+// allocate device memory.
+//
+// Who needs this: code that runs where cudaMalloc is not an option -- inside
+// a CUDA stream capture (allocation is not a capturable operation), under a
+// framework that has reserved the device memory for its own caching allocator
+// and forbids foreign allocations, or in a process that must not grow its
+// footprint after start-up.  Such a caller already holds the rotated queries,
+// the gathered key/value context and the output buffer; what the attention
+// kernel still needs is scratch for the partial results of key-range splits.
+// Here that scratch is one file-scope device array of fixed size, created when
+// the library's module is loaded on a device and held until the process
+// exits.
+//
+// Set-up: the first call on a device (with that device current) loads this
+// module, takes the array's device address with cudaGetSymbolAddress and sets
+// the attention kernel's shared-memory attribute.  Make that first call before
+// any stream capture.  Later calls only enqueue work.
+//
+// Sharing: every call on a device uses the same array and leaves its contents
+// there.  Split partials are fully rewritten by each call before they are read;
+// the kernel's error word (the array's first bytes) is cleared on the call's
+// stream.  Calls whose kernels overlap on the GPU (different streams without
+// ordering) race on the array and give undefined output.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ff.h"
+#include "ff_internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FF_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kErrBytes = 256;  // error word area at the start of the array
+
+std::mutex g_mu;
+void* g_scratch[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Same cost model as the bank path, restricted to real splits (s >= 2).
+int split_for(int units, int n_kv, int sms) {
+  if (n_kv < 2) return 1;
+  double best = 1e300;
+  int best_s = 2;
+  for (int s = 2; s <= (n_kv < 4 ? n_kv : 4); ++s) {
+    const long long pieces = static_cast<long long>(units) * s;
+    const long long waves = (pieces + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+int setup(int dev, void** scratch, int* sms) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch[dev]) {
+    int major = 0, minor = 0, count = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FF_ERR_CUDA;
+    if (major != 10 || minor != 3) return FF_ERR_UNSUPPORTED;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q{};
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return FF_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return FF_ERR_CUDA;
+    }
+    if (ff::attention_configure(64) != cudaSuccess || ff::attention_configure(128) != cudaSuccess) return FF_ERR_CUDA;
+    g_sms[dev] = count;
+    g_scratch[dev] = p;
+  }
+  *scratch = g_scratch[dev];
+  *sms = g_sms[dev];
+  return FF_OK;
+}
+
+int map2d(CUtensorMap* map, const void* base, int rows, int heads, int d) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * d, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? FF_OK
+             : FF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v, void* out, int nq, int nk, int heads,
+                                    int head_dim, void* stream) {
+  if (!q || !k || !v || !out || nq < 1 || nk < 1 || heads < 1 || (head_dim != 64 && head_dim != 128))
+    return FF_ERR_ARG;
+  for (const void* p : {q, k, v, static_cast<const void*>(out)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return FF_ERR_ARG;
+  const int n_qb = (nq + 255) / 256;
+  const long long n_kv = (static_cast<long long>(nk) + 127) / 128;
+  if (n_kv > (1 << 24) || static_cast<long long>(heads) * n_qb > (1 << 24)) return FF_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FF_ERR_CUDA;
+  void* scratch = nullptr;
+  int sms = 0;
+  const int rc = setup(dev, &scratch, &sms);
+  if (rc != FF_OK) return rc;
+
+  ff::AttnParams ap{};
+  ap.out = out;
+  ap.nq = nq;
+  ap.nk = nk;
+  ap.heads = heads;
+  ap.n_qb = n_qb;
+  ap.n_kv = static_cast<int>(n_kv);
+  ap.n_split = split_for(heads * n_qb, ap.n_kv, sms);
+  ap.n_pieces = heads * n_qb * ap.n_split;
+  const size_t part_rows = static_cast<size_t>(ap.n_pieces) * 256;
+  const size_t need = kErrBytes + part_rows * static_cast<size_t>(head_dim) * 4 + part_rows * 8;
+  if (ap.n_split > 1 && need > FF_NOALLOC_SCRATCH_BYTES) return FF_ERR_ARG;  // beyond the static scratch
+  unsigned char* base = static_cast<unsigned char*>(scratch);
+  ap.err = reinterpret_cast<unsigned int*>(base);
+  ap.part_o = reinterpret_cast<float*>(base + kErrBytes);
+  ap.part_ml = reinterpret_cast<float*>(base + kErrBytes + part_rows * head_dim * 4);
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / __builtin_sqrt(static_cast<double>(head_dim)));
+
+  CUtensorMap tq, tk, tv;
+  if (map2d(&tq, q, nq, heads, head_dim) != FF_OK || map2d(&tk, k, nk, heads, head_dim) != FF_OK ||
+      map2d(&tv, v, nk, heads, head_dim) != FF_OK)
+    return FF_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ap.err, 0, sizeof(unsigned int), s) != cudaSuccess) return FF_ERR_CUDA;
+  const int grid = ap.n_pieces < sms ? ap.n_pieces : sms;
+  if (ff::launch_attention(head_dim, tq, tk, tv, ap, grid, s) != cudaSuccess) return FF_ERR_CUDA;
+  if (ap.n_split > 1 && ff::launch_combine(head_dim, ap, s) != cudaSuccess) return FF_ERR_CUDA;
+  return FF_OK;
+}

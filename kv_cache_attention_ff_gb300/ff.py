@@ -24,6 +24,7 @@ EXPORTS = [
     "ff_desc_default", "ff_bank_create", "ff_anchor_publish", "ff_render_attn", "ff_bank_destroy",
     "ff_bank_gamma", "ff_bank_slot_info", "ff_bank_bytes", "ff_bank_error_poll", "ff_status_string",
     "ff_plan_chunk", "ff_bank_set_timing", "ff_bank_read_timing", "ff_render_kernel_count",
+    "ff_attention_noalloc",
 ]
 
 
@@ -83,6 +84,7 @@ def _lib():
         lib.ff_bank_set_timing.argtypes = [P, I]
         lib.ff_bank_read_timing.argtypes = [P, ctypes.POINTER(KernelTimes)]
         lib.ff_render_kernel_count.argtypes = [P, I, ctypes.POINTER(I)]
+        lib.ff_attention_noalloc.argtypes = [V, V, V, V, I, I, I, I, V]
         for name in EXPORTS:
             if name != "ff_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -114,6 +116,16 @@ def plan_chunk(desc: BankDesc, chunk: int) -> ChunkPlan:
     p = ChunkPlan()
     _check(_lib().ff_plan_chunk(ctypes.byref(desc), chunk, ctypes.byref(p)), "ff_plan_chunk")
     return p
+
+
+def attention_noalloc(q, k, v, out, stream=None):
+    """Attention over a caller-held context without any device allocation
+    (see ff_attention_noalloc in include/ff.h)."""
+    nq, heads, d = q.shape
+    nk = k.shape[0]
+    _check(_lib().ff_attention_noalloc(_ptr(q, (nq, heads, d), "q"), _ptr(k, (nk, heads, d), "k"),
+                                       _ptr(v, (nk, heads, d), "v"), _ptr(out, (nq, heads, d), "out"),
+                                       nq, nk, heads, d, _stream(stream, q.device)), "ff_attention_noalloc")
 
 
 class _DevView:
