@@ -34,6 +34,25 @@ METRIC = "Renderer bank-attention TFLOP/s (% BF16 peak) and chunk-steps/s on 1 G
 WORKLOAD = "wan13b_480p"   # 12 heads, d 128, 30x52 tokens/frame, chunk 3 frames, H 5, 2 anchors
 LAYERS_PER_CHUNK_STEP = 30  # Wan2.1-1.3B transformer blocks: a chunk-step runs every layer once
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the
+# steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
+# a kernel edited since then reports null.
+NCU_TRAFFIC = {
+    "bank_attn_kernel": (249.6e6, "ff_attn.cu", "25b0ad46f4b628a4"),
+    "publish_gather_kernel": (382.1e6, "ff_publish.cu", "922aef267f376fa4"),
+}
+
+
+def ncu_traffic(kernel):
+    import hashlib
+    nbytes, src, digest = NCU_TRAFFIC[kernel]
+    path = os.path.join(ROOT, "kv_cache_attention_ff_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            now = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if now == digest else None
 
 
 def load_peaks():
@@ -239,11 +258,11 @@ def run_gpu(args):
     pub_gbs = g1_bytes / (pub_ms * 1e-3) / 1e9
     roofline = {"kernel": "bank_attn_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
-                "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "traffic": ncu_traffic("bank_attn_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "algorithmic_per_launch": f"{flops / 1e9:.1f} GFLOP (4*Nq*Nk*d*h)", "avg_launch_ms": round(attn_ms, 4)}
     roofline_publish = {"kernel": "publish_gather_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
-                        "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                        "traffic": ncu_traffic("publish_gather_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} hbm_gbs",
                         "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (92 frames x 4.79 MB)",
                         "avg_launch_ms": round(pub_ms, 4)}
 
@@ -277,27 +296,28 @@ def run_gpu(args):
 
 
 def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
-    """Same calls through the public API with host buffers: H2D of q, k, v and D2H of
-    the output inside the timed region.  Uses fresh (layer) banks' later chunks."""
+    """Same calls through the public API with host buffers.  Every step copies
+    its q, k, v from pinned host memory to the device and its output back to
+    pinned host memory inside the timed region.  Copies run on their own
+    streams with double-buffered device staging, so step j+1's upload and
+    step j-1's download overlap step j's kernels."""
     import torch
 
     from kv_cache_attention_ff_gb300 import ff
     T, H, D = 1560, 12, 128
     nq = 3 * T
     host_in = [[t.cpu().pin_memory() for t in pool[s][0]] for s in range(4)]
-    host_out = torch.empty((nq, H, D), dtype=torch.bfloat16).pin_memory()
-    dq = torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev)
-    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
-    # a separate bank so the contract (sequential chunks) holds
-    steps = args.steps
-    warm = args.warmup
+    host_out = [torch.empty((nq, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dbuf = [[torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)] for _ in range(2)]
+    dout = [torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    steps, warm = args.steps, args.warmup
     layers = max(1, math.ceil((steps + warm) / 88))
     eb = ff.Bank(n_layers=layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
                  total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, device=dev.index)
-    z = torch.zeros((9 * T, H, D), dtype=torch.bfloat16, device=dev)
+    z = torch.zeros((3 * T, H, D), dtype=torch.bfloat16, device=dev)
     for layer in range(layers):
         for b in range(3):
-            eb.anchor_publish(layer, 30 * b, 3, z[: 3 * T], z[: 3 * T], stream)
+            eb.anchor_publish(layer, 30 * b, 3, z, z, stream)
         for st in range(4):
             for i in range(5):
                 q, k, v = pool[st][i % 4]
@@ -310,36 +330,54 @@ def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
             if nxt[key] < 27 and len(calls) < steps + warm:
                 calls.append((key[0], key[1], nxt[key]))
                 nxt[key] += 1
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    uploaded = [ev(), ev()]
+    computed = [ev(), ev()]
+    downloaded = [ev(), ev()]
+    started = [False, False]
 
     def step(j):
+        b = j & 1
         layer, st, c = calls[j]
-        hq, hk, hv = host_in[st]
-        with torch.cuda.stream(stream):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-        rc = eb.render_attn_raw(layer, st, c, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), out.data_ptr(),
+        if started[b]:
+            up.wait_event(computed[b])          # staging buffer b is free once step j-2 ran
+        with torch.cuda.stream(up):
+            for dst, src in zip(dbuf[b], host_in[st]):
+                dst.copy_(src, non_blocking=True)
+            uploaded[b].record(up)
+        stream.wait_event(uploaded[b])
+        if started[b]:
+            stream.wait_event(downloaded[b])    # output buffer b was read back
+        dq, dk, dv = dbuf[b]
+        rc = eb.render_attn_raw(layer, st, c, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dout[b].data_ptr(),
                                 stream.cuda_stream)
         if rc != 0:
             raise RuntimeError(f"ff_render_attn failed with status {rc}")
-        with torch.cuda.stream(stream):
-            host_out.copy_(out, non_blocking=True)
+        computed[b].record(stream)
+        down.wait_event(computed[b])
+        with torch.cuda.stream(down):
+            host_out[b].copy_(dout[b], non_blocking=True)
+            downloaded[b].record(down)
+        started[b] = True
 
     for j in range(warm):
         step(j)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(up)
     for j in range(warm, warm + steps):
         step(j)
-    e1.record(stream)
+    e1.record(down)  # every upload precedes its kernels, which precede the download on `down`
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     eb.close()
     bytes_in = 3 * nq * H * D * 2
     return {"value": round(flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_in,
-            "d2h_bytes_per_step": nq * H * D * 2, "ms_per_step": round(ms / steps, 4)}
+            "d2h_bytes_per_step": nq * H * D * 2, "ms_per_step": round(ms / steps, 4),
+            "copies": "pinned host <-> device every step, double-buffered on two copy streams"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -369,14 +407,16 @@ def oracle_sample(rows: int, heads: int, seed: int = 0):
 
 
 def cpu_baseline(budget_s: float = 15.0):
-    # calibrate on a small sample, then size the timed sample to about budget_s
-    dt0, f0 = oracle_sample(128, 1)
+    # calibrate on a small sample, then size the timed sample (rows x heads) to about budget_s
+    dt0, f0 = oracle_sample(512, 1)
     rate = f0 / max(dt0, 1e-6)
-    rows = int(min(4680, max(128, budget_s * rate / (4.0 * 31200 * 128))))
-    dt, fl = oracle_sample(rows, 1, seed=1)
+    per_head = 4.0 * 4680 * 31200 * 128
+    heads = int(min(12, max(1, budget_s * rate // per_head)))
+    rows = 4680 if heads > 1 else int(min(4680, max(128, budget_s * rate / (4.0 * 31200 * 128))))
+    dt, fl = oracle_sample(rows, heads, seed=1)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle attention of {rows} query rows x 1 head over the 31200 keys of the "
-                      f"steady 1.3B call ({fl / 1e9:.1f} GFLOP, {dt:.1f} s); rope/publish/gather not included"}
+            "sample": f"fp64 numpy oracle attention of {rows} query rows x {heads} heads over the 31200 keys of "
+                      f"the steady 1.3B call ({fl / 1e9:.1f} GFLOP, {dt:.1f} s); rope/publish/gather not included"}
 
 
 def run_reference(args):

@@ -175,6 +175,15 @@ int ff_bank_read_timing(ff_bank_t* bank, ff_kernel_times* out);
 /* Number of kernels one ff_render_attn call of `chunk` launches (2 or 3). */
 int ff_render_kernel_count(const ff_bank_t* bank, int chunk, int* count);
 
+/* ---- self-test of failure detection ----
+ *
+ * Enqueue one small kernel whose bounded wait can never be satisfied: it
+ * gives up after limit_ms (1..10000) and sets the bank's device error word,
+ * exactly as a render kernel does when one of its waits runs out.  Used to
+ * test that ff_bank_error_poll reports FF_ERR_DEVICE_TIMEOUT without
+ * faulting or hanging the GPU; the context stays usable afterwards. */
+int ff_bank_wait_probe(ff_bank_t* bank, int limit_ms, void* stream);
+
 /* ---- attention without any device allocation ----
  *
  * The pages have no counterpart of this entry point.  It serves callers that

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libff.so")
 
-SOURCES = ["ff_bank.cpp", "ff_publish.cu", "ff_attn.cu", "ff_noalloc.cu"]
+SOURCES = ["ff_bank.cpp", "ff_publish.cu", "ff_attn.cu", "ff_noalloc.cu", "ff_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -726,6 +726,14 @@ int ff_render_kernel_count(const ff_bank_t* b, int chunk, int* count) {
   return FF_OK;
 }
 
+int ff_bank_wait_probe(ff_bank_t* b, int limit_ms, void* stream) {
+  if (!b || limit_ms < 1 || limit_ms > 10000) return FF_ERR_ARG;
+  if (cudaSetDevice(b->d.device) != cudaSuccess) return FF_ERR_CUDA;
+  return cuda_err(launch_wait_probe(b->err, static_cast<unsigned long long>(limit_ms) * 1000000ull,
+                                    static_cast<cudaStream_t>(stream)),
+                  "wait probe launch");
+}
+
 int ff_bank_set_timing(ff_bank_t* b, int enable) {
   if (!b) return FF_ERR_ARG;
   cudaSetDevice(b->d.device);

@@ -75,6 +75,7 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensor
                              const AttnParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s);
 size_t attention_smem_bytes(int head_dim);
+cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t attention_configure(int head_dim);
 
 }  // namespace ff

@@ -24,7 +24,7 @@ EXPORTS = [
     "ff_desc_default", "ff_bank_create", "ff_anchor_publish", "ff_render_attn", "ff_bank_destroy",
     "ff_bank_gamma", "ff_bank_slot_info", "ff_bank_bytes", "ff_bank_error_poll", "ff_status_string",
     "ff_plan_chunk", "ff_bank_set_timing", "ff_bank_read_timing", "ff_render_kernel_count",
-    "ff_attention_noalloc",
+    "ff_attention_noalloc", "ff_bank_wait_probe",
 ]
 
 
@@ -85,6 +85,7 @@ def _lib():
         lib.ff_bank_read_timing.argtypes = [P, ctypes.POINTER(KernelTimes)]
         lib.ff_render_kernel_count.argtypes = [P, I, ctypes.POINTER(I)]
         lib.ff_attention_noalloc.argtypes = [V, V, V, V, I, I, I, I, V]
+        lib.ff_bank_wait_probe.argtypes = [P, I, V]
         for name in EXPORTS:
             if name != "ff_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -229,6 +230,10 @@ class Bank:
 
     def error_poll(self):
         return _lib().ff_bank_error_poll(self.handle)
+
+    def wait_probe(self, limit_ms: int, stream=None):
+        """Enqueue the failure-detection self-test (a wait that times out)."""
+        _check(_lib().ff_bank_wait_probe(self.handle, limit_ms, _stream(stream, self.device)), "ff_bank_wait_probe")
 
     def set_timing(self, enable: bool):
         _check(_lib().ff_bank_set_timing(self.handle, int(enable)), "ff_bank_set_timing")
