@@ -148,6 +148,19 @@ def dist_setup():
     return world, rank, local
 
 
+def aggregate(ms_local, work_per_rank, world, pg=None, device=None):
+    """Whole-job throughput of N replicas: the timed interval is the maximum over
+    ranks, the work is the sum (every rank does the same work).  Returns
+    (max interval in ms, work units per second / 1e12)."""
+    import torch
+    ms = float(ms_local)
+    if pg is not None and world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, work_per_rank * world / (ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args):
@@ -243,12 +256,8 @@ def run_gpu(args):
     kt = bank.read_timing()
     bank.set_timing(False)
     assert bank.error_poll() == 0, "device-side wait timed out"
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, value = aggregate(ms_total, flops * args.steps, world, pg, dev)
     ms_step = ms_total / args.steps
-    value = flops * args.steps * world / (ms_total * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
     attn_ms = kt.attn_ms / max(kt.calls, 1)
