@@ -278,6 +278,8 @@ def run_gpu(args):
     # end to end: pinned host inputs -> device, call, output -> pinned host, every step
     e2e = None if args.no_e2e else run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
 
+    planner = None if args.no_e2e else run_planner(stream, args, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_budget)
@@ -296,12 +298,50 @@ def run_gpu(args):
             "kernel_ms": {"publish_gather": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def run_planner(stream, args, dev):
+    """Planner-role attention at the W_ctx-wide block: 261 latents of the 1.3B 480p
+    shape, block 8 over the clean KV of blocks 2..7 plus itself (21 frames)."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff, synth
+    T, H, D = 1560, 12, 128
+    pb = ff.Bank(n_layers=1, n_stages=1, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=27,
+                 total_frames=261, heads=H, head_dim=D, frame_h=30, frame_w=52, planner_block=3, planner_history=6,
+                 device=dev.index)
+    with torch.cuda.stream(stream):
+        ka = synth.device_frames(6, 0, synth.ANCHOR_STREAM, synth.K, list(range(60, 240, 10)), T, H, D, "ar",
+                                 device=dev)
+        va = synth.device_frames(6, 0, synth.ANCHOR_STREAM, synth.V, list(range(60, 240, 10)), T, H, D, "normal",
+                                 device=dev)
+        q, k, v = (synth.device_frames(6, 0, 51, t, [240, 250, 260], T, H, D, "ar" if t < 2 else "normal",
+                                       device=dev) for t in range(3))
+    torch.cuda.synchronize()
+    pb.anchor_publish(0, 60, 18, ka, va, stream)
+    out = torch.empty_like(q)
+    for _ in range(args.warmup):
+        pb.planner_attn(0, 8, q, k, v, out, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        pb.planner_attn(0, 8, q, k, v, out, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert pb.error_poll() == 0
+    pb.close()
+    flops = 4.0 * 4680 * 21 * T * D * H
+    return {"workload": "planner block, 1.3B 480p shape, 21 context frames (W_ctx)", "queries": 4680,
+            "keys": 21 * T, "ms_per_call": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
 
 
 def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):

@@ -72,6 +72,8 @@ typedef struct ff_bank_desc {
   double rope_theta;    /* rotary base theta (10000) */
   size_t max_bytes;     /* 0 = unlimited; otherwise create fails with FF_ERR_OOM above this many device bytes */
   int device;           /* CUDA device ordinal */
+  int planner_block;    /* B_P: anchors per planner block (default 3) */
+  int planner_history;  /* H_P: previous planner blocks a planner block attends to (default 6; 0 = no planner scratch) */
 } ff_bank_desc;
 
 typedef struct ff_bank ff_bank_t;
@@ -111,6 +113,23 @@ int ff_anchor_publish(ff_bank_t* bank, int layer, int first_anchor_frame, int n_
  * not resident. */
 int ff_render_attn(ff_bank_t* bank, int layer, int stage, int chunk,
                    const void* q_pre, const void* k_pre, const void* v, void* out, void* stream);
+
+/* Planner-role attention of planner block `block` of `layer`
+ * (onedev.kr/papers/332, "무엇과 다른가": the planner produces the clean anchors
+ * B_P = 3 at a time with history H_P = 6 and context budget W_ctx = 21;
+ * "어떻게 쓰나": planner blocks attend causally to the clean KV of previous
+ * blocks).  Block b holds anchors b*B_P .. b*B_P + B_P - 1 (frames a*Delta;
+ * fewer in the last block).  q_pre, k_pre, v: device bf16
+ * [n_b * T, heads, head_dim] for the block's n_b anchor frames, before rotary
+ * encoding; out: same shape, out = softmax(RoPE(Q) K_ctx^T / sqrt(d)) V_ctx
+ * with context [clean anchor KV of blocks max(0, b - H_P) .. b-1, oldest first;
+ * the block itself], i.e. at most H_P * B_P + B_P = W_ctx frames.  Nothing is
+ * published: the block's clean KV enters the anchor ring through
+ * ff_anchor_publish once the block is done.  Errors: FF_ERR_ARG (block out of
+ * range, planner_history == 0), FF_ERR_ANCHOR_MISSING if an anchor of the
+ * history blocks is not resident (size anchor_capacity >= H_P * B_P). */
+int ff_planner_attn(ff_bank_t* bank, int layer, int block, const void* q_pre, const void* k_pre, const void* v,
+                    void* out, void* stream);
 
 /* Wait for all work the bank enqueued, then free everything.  NULL-safe. */
 int ff_bank_destroy(ff_bank_t* bank);
@@ -155,6 +174,18 @@ typedef struct ff_chunk_plan {
 
 /* Chunk plan of `chunk` for a description (FF_ERR_ARG past the last chunk). */
 int ff_plan_chunk(const ff_bank_desc* desc, int chunk, ff_chunk_plan* out);
+
+typedef struct ff_planner_plan {
+  int first_anchor;     /* first anchor index of the block (frame = index * Delta) */
+  int n_anchors;        /* anchors in the block (B_P, fewer at the end) */
+  int hist_first_block; /* oldest history block */
+  int n_hist_blocks;    /* min(block, H_P) */
+  int hist_frames;      /* anchor frames of the history blocks */
+  int key_frames;       /* hist_frames + n_anchors */
+} ff_planner_plan;
+
+/* Plan of planner block `block` (FF_ERR_ARG past the last block). */
+int ff_plan_planner_block(const ff_bank_desc* desc, int block, ff_planner_plan* out);
 
 /* ---- timing of the library's own kernels (CUDA events on the call's stream) ---- */
 

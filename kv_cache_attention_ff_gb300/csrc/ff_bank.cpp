@@ -78,6 +78,8 @@ struct ff_bank {
     float* part_ml = nullptr;
   };
   std::vector<Scratch> scratch;  // per stage
+  Scratch planner;               // planner blocks (when planner_history > 0)
+  int planner_max_pieces = 0;
   double2* rope64 = nullptr;
   float2* rope32 = nullptr;
   int rope_y_base = 0, rope_x_base = 0, pt = 0, py = 0, px = 0;
@@ -95,6 +97,9 @@ struct ff_bank {
   std::vector<cudaEvent_t> ev_anchor;      // [cap] after the latest publish touching the slot
   std::vector<cudaStream_t> anchor_stream;
   std::vector<bool> anchor_used;
+  cudaEvent_t ev_planner = nullptr;        // after the latest planner call
+  cudaStream_t planner_stream = nullptr;
+  bool planner_used = false;
 
   // timing
   bool timing = false;
@@ -136,11 +141,15 @@ int validate_desc(const ff_bank_desc* d) {
       d->device < 0)
     return FF_ERR_ARG;
   if (2 + (d->history + 1) * d->chunk_frames > kMaxItems) return FF_ERR_ARG;
+  if (d->planner_block < 1 || d->planner_block > 8 || d->planner_history < 0 ||
+      (d->planner_history + 1) * d->planner_block > kMaxItems)
+    return FF_ERR_ARG;
   const long long T = static_cast<long long>(d->frame_h) * d->frame_w;
   const long long upf = T * d->heads * d->head_dim / 8;
   // every count the kernels index with 32-bit ints must fit
   if (upf * (2 + (d->history + 1) * d->chunk_frames) > (1ll << 31) - 1) return FF_ERR_ARG;
   if (T * (2 + (d->history + 1) * d->chunk_frames) > (1ll << 30)) return FF_ERR_ARG;
+  if (upf * (d->planner_history + 1) * d->planner_block > (1ll << 31) - 1) return FF_ERR_ARG;
   if (static_cast<long long>(d->heads) * d->head_dim * 2 % 16 != 0) return FF_ERR_ARG;
   return FF_OK;
 }
@@ -169,6 +178,20 @@ void plan(const ff_bank_desc& d, int i, ff_chunk_plan* p) {
   p->hist_frames = hf;
   p->slot = i % d.history;
   p->key_frames = p->n_anchors + hf + p->n_frames;
+}
+
+int n_anchor_frames(const ff_bank_desc& d) { return (d.total_frames - 1) / d.anchor_stride + 1; }
+int n_planner_blocks(const ff_bank_desc& d) { return (n_anchor_frames(d) + d.planner_block - 1) / d.planner_block; }
+
+// Planner block b: anchors b*B_P .. b*B_P + n - 1; history = the anchors of blocks
+// max(0, b - H_P) .. b - 1, all full blocks.
+void plan_planner(const ff_bank_desc& d, int b, ff_planner_plan* p) {
+  p->first_anchor = b * d.planner_block;
+  p->n_anchors = std::min(d.planner_block, n_anchor_frames(d) - p->first_anchor);
+  p->hist_first_block = std::max(0, b - d.planner_history);
+  p->n_hist_blocks = b - p->hist_first_block;
+  p->hist_frames = p->n_hist_blocks * d.planner_block;
+  p->key_frames = p->hist_frames + p->n_anchors;
 }
 
 // Key-range splits per (head, query block) so that pieces fill the SMs:
@@ -221,6 +244,8 @@ void free_all(ff_bank* b) {
     if (e) cudaEventDestroy(e);
   for (auto& tc : b->timed)
     for (cudaEvent_t e : tc.ev) cudaEventDestroy(e);
+  if (b->ev_planner) cudaEventDestroy(b->ev_planner);
+  b->ev_planner = nullptr;
   b->ev_stage.clear();
   b->ev_anchor.clear();
   b->timed.clear();
@@ -269,6 +294,8 @@ int ff_desc_default(ff_bank_desc* d) {
   d->rope_theta = 10000.0;
   d->max_bytes = 0;
   d->device = 0;
+  d->planner_block = 3;
+  d->planner_history = 6;
   return FF_OK;
 }
 
@@ -317,17 +344,23 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   b->max_key_frames = 2 + (d.history + 1) * d.chunk_frames;
 
   // attention split scratch: the largest piece count any call of this bank can use
-  int max_pieces = 0;
-  for (int f = 1; f <= d.chunk_frames; ++f) {
-    const int nq = static_cast<int>(f * T);
-    const int n_qb = (nq + kQBlock - 1) / kQBlock;
-    for (int kf = f; kf <= b->max_key_frames; ++kf) {
-      const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile);
-      const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
-      if (s > 1) max_pieces = std::max(max_pieces, d.heads * n_qb * s);
+  auto pieces_cap = [&](int q_frames, int k_frames) {
+    int m = 0;
+    for (int f = 1; f <= q_frames; ++f) {
+      const int nq = static_cast<int>(f * T);
+      const int n_qb = (nq + kQBlock - 1) / kQBlock;
+      for (int kf = f; kf <= k_frames; ++kf) {
+        const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile);
+        const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
+        if (s > 1) m = std::max(m, d.heads * n_qb * s);
+      }
     }
-  }
+    return m;
+  };
+  const int max_pieces = pieces_cap(d.chunk_frames, b->max_key_frames);
   b->max_pieces = max_pieces;
+  const int planner_frames = (d.planner_history + 1) * d.planner_block;
+  b->planner_max_pieces = d.planner_history > 0 ? pieces_cap(d.planner_block, planner_frames) : 0;
 
   const int pt = (d.head_dim - 4 * (d.head_dim / 6)) / 2;
   const int py = (d.head_dim / 6);
@@ -347,7 +380,13 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   const size_t part_ml_bytes = static_cast<size_t>(max_pieces) * kQBlock * 8;
   const size_t per_stage = 2 * ctx_bytes + qrot_bytes + part_o_bytes + part_ml_bytes;
   const size_t rope_bytes = n_rope * (sizeof(double2) + sizeof(float2));
-  b->total_bytes = stage_bytes + anchor_bytes + d.n_stages * per_stage + rope_bytes + 256;
+  const size_t pl_ctx_bytes = static_cast<size_t>(planner_frames) * b->frame_bytes;
+  const size_t pl_qrot_bytes = static_cast<size_t>(d.planner_block) * b->frame_bytes;
+  const size_t pl_part_o_bytes = static_cast<size_t>(b->planner_max_pieces) * kQBlock * d.head_dim * 4;
+  const size_t pl_part_ml_bytes = static_cast<size_t>(b->planner_max_pieces) * kQBlock * 8;
+  const size_t planner_bytes =
+      d.planner_history > 0 ? 2 * pl_ctx_bytes + pl_qrot_bytes + pl_part_o_bytes + pl_part_ml_bytes : 0;
+  b->total_bytes = stage_bytes + anchor_bytes + d.n_stages * per_stage + planner_bytes + rope_bytes + 256;
   if (d.max_bytes && b->total_bytes > d.max_bytes) {
     FF_LOG("bank needs %zu bytes > max_bytes %zu", b->total_bytes, d.max_bytes);
     delete b;
@@ -372,6 +411,18 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
     b->scratch[k].part_o = static_cast<float*>(p);
     if ((rc = alloc(b, part_ml_bytes, &p)) != FF_OK) goto fail;
     b->scratch[k].part_ml = static_cast<float*>(p);
+  }
+  if (d.planner_history > 0) {
+    if ((rc = alloc(b, pl_ctx_bytes, &p)) != FF_OK) goto fail;
+    b->planner.ctx_k = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, pl_ctx_bytes, &p)) != FF_OK) goto fail;
+    b->planner.ctx_v = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, pl_qrot_bytes, &p)) != FF_OK) goto fail;
+    b->planner.q_rot = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, pl_part_o_bytes, &p)) != FF_OK) goto fail;
+    b->planner.part_o = static_cast<float*>(p);
+    if ((rc = alloc(b, pl_part_ml_bytes, &p)) != FF_OK) goto fail;
+    b->planner.part_ml = static_cast<float*>(p);
   }
   if ((rc = alloc(b, n_rope * sizeof(double2), &p)) != FF_OK) goto fail;
   b->rope64 = static_cast<double2*>(p);
@@ -439,6 +490,10 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
       rc = FF_ERR_CUDA;
       goto fail;
     }
+  if (cudaEventCreateWithFlags(&b->ev_planner, cudaEventDisableTiming) != cudaSuccess) {
+    rc = FF_ERR_CUDA;
+    goto fail;
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) {
     rc = FF_ERR_CUDA;
     goto fail;
@@ -549,8 +604,9 @@ int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_p
     it.t = a;
     it.old_ctx = -1;
   }
-  // The slots may still be read by renders on other streams.
+  // The slots may still be read by renders or planner blocks on other streams.
   wait_stage_events(b, s, -1);
+  if (b->planner_used && b->planner_stream != s) cudaStreamWaitEvent(s, b->ev_planner, 0);
   int rc = cuda_err(launch_publish(prm, 0, s), "anchor publish launch");
   if (rc != FF_OK) return rc;
   for (int j = 0; j < n; ++j) {
@@ -710,6 +766,109 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   own.tag = chunk;
   own.frames = pl.n_frames;
   ++next;
+  return FF_OK;
+}
+
+int ff_plan_planner_block(const ff_bank_desc* d, int block, ff_planner_plan* out) {
+  if (validate_desc(d) != FF_OK || !out || block < 0 || block >= n_planner_blocks(*d)) return FF_ERR_ARG;
+  plan_planner(*d, block, out);
+  return FF_OK;
+}
+
+int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const void* k_pre, const void* v,
+                    void* out, void* stream) {
+  if (!b || b->d.planner_history < 1 || layer < 0 || layer >= b->d.n_layers || block < 0 ||
+      block >= n_planner_blocks(b->d) || !q_pre || !k_pre || !v || !out || !aligned16(q_pre) ||
+      !aligned16(k_pre) || !aligned16(v) || !aligned16(out))
+    return FF_ERR_ARG;
+  const ff_bank_desc& d = b->d;
+  ff_planner_plan pl;
+  plan_planner(d, block, &pl);
+  const int n_hist = pl.hist_frames;
+  std::vector<int> hslots(n_hist);
+  for (int j = 0; j < n_hist; ++j) {
+    const int a = (pl.hist_first_block * d.planner_block + j) * d.anchor_stride;
+    hslots[j] = (a / d.anchor_stride) % d.anchor_capacity;
+    if (b->aslot(layer, hslots[j]).tag != a) return FF_ERR_ANCHOR_MISSING;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
+  ff_bank::Scratch& sc = b->planner;
+
+  G1Params prm{};
+  prm.q_in = q_pre;
+  prm.k_in = k_pre;
+  prm.v_in = v;
+  prm.q_rot = sc.q_rot;
+  prm.ctx_k = sc.ctx_k;
+  prm.ctx_v = sc.ctx_v;
+  prm.rope64 = b->rope64;
+  prm.rope32 = b->rope32;
+  prm.y_base = b->rope_y_base;
+  prm.x_base = b->rope_x_base;
+  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
+  prm.units_per_row = d.heads * d.head_dim / 8;
+  prm.units_per_head = d.head_dim / 8;
+  prm.frame_w = d.frame_w;
+  prm.pt = b->pt;
+  prm.py = b->py;
+  prm.px = b->px;
+  int n_items = 0;
+  for (int j = 0; j < n_hist; ++j) {
+    G1Item& it = prm.items[n_items++];
+    it.kind = kItemCopy;
+    it.k = b->anchor_k(layer, hslots[j]);
+    it.v = b->anchor_v(layer, hslots[j]);
+    it.ctx = j;
+    it.r = it.t = 0;
+    it.old_ctx = -1;
+  }
+  for (int r = 0; r < pl.n_anchors; ++r) {
+    G1Item& it = prm.items[n_items++];
+    it.kind = kItemOwnCtx;
+    it.k = nullptr;
+    it.v = nullptr;
+    it.ctx = n_hist + r;
+    it.r = r;
+    it.t = (pl.first_anchor + r) * d.anchor_stride;
+    it.old_ctx = -1;
+  }
+  prm.n_items = n_items;
+
+  const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
+  const int nq = static_cast<int>(pl.n_anchors * T);
+  const int nk = static_cast<int>(pl.key_frames * T);
+  AttnParams ap{};
+  ap.out = out;
+  ap.err = b->err;
+  ap.nq = nq;
+  ap.nk = nk;
+  ap.heads = d.heads;
+  ap.n_qb = (nq + kQBlock - 1) / kQBlock;
+  ap.n_kv = (nk + kKTile - 1) / kKTile;
+  ap.n_split = choose_split(d.heads * ap.n_qb, ap.n_kv, b->sm_count);
+  if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->planner_max_pieces) ap.n_split = 1;
+  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
+  ap.part_o = sc.part_o;
+  ap.part_ml = sc.part_ml;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map(b, &tq, sc.q_rot, nq)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tk, sc.ctx_k, nk)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tv, sc.ctx_v, nk)) != FF_OK) return rc;
+
+  if (b->planner_used && b->planner_stream != s) cudaStreamWaitEvent(s, b->ev_planner, 0);
+  for (int j = 0; j < n_hist; ++j)
+    if (b->anchor_used[hslots[j]] && b->anchor_stream[hslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[hslots[j]], 0);
+  if ((rc = cuda_err(launch_publish(prm, 0, s), "planner gather launch")) != FF_OK) return rc;
+  const int grid = std::min(ap.n_pieces, b->sm_count);
+  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "planner attention launch")) != FF_OK)
+    return rc;
+  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "planner combine launch")) != FF_OK) return rc;
+  cudaEventRecord(b->ev_planner, s);
+  b->planner_stream = s;
+  b->planner_used = true;
   return FF_OK;
 }
 

@@ -18,6 +18,7 @@ enum ItemKind : int {
   kItemCopy = 0,    // context frame <- (k, v) source frame (anchor or history slot)
   kItemOwn = 1,     // own chunk frame r: RoPE(q) -> q_rot, RoPE(k) and v -> slot frame r and context
   kItemAnchor = 2,  // anchor input frame r: RoPE(k) and v -> anchor slot
+  kItemOwnCtx = 3,  // like kItemOwn but nothing is published (planner blocks)
 };
 
 struct G1Item {

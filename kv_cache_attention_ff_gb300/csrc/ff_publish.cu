@@ -9,6 +9,10 @@
 //   * RoPE of the chunk's K under the published-K contract (below) and the
 //     store of (K, V) into bank slot i mod H;
 //   * the gather of [anchors; history; own] K/V into one contiguous context.
+// The same kernel serves anchor publishes (rotate at the anchor frame and store
+// into the anchor ring) and planner blocks (rotate the block and gather it after
+// the clean KV of the previous blocks, publishing nothing: the planner's clean
+// KV is published later by the block's cache-extraction forward).
 // The slot being overwritten still holds chunk i-H, which chunk i attends to:
 // the thread that writes unit u of the new chunk first reads unit u of the old
 // one and saves it into the context, so the read precedes the write in one
@@ -154,9 +158,10 @@ __global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __gri
     return;
   }
 
-  // Own-chunk frame or anchor frame.
-  const bool own = (kind == kItemOwn);
-  const bool save_old = own && I.old_ctx >= 0;
+  // Own-chunk frame, planner-block frame or anchor frame.
+  const bool own = (kind == kItemOwn) || (kind == kItemOwnCtx);
+  const bool to_slot = (kind != kItemOwnCtx);
+  const bool save_old = (kind == kItemOwn) && I.old_ctx >= 0;
   const size_t in_base = static_cast<size_t>(I.r) * upf;
 #pragma unroll
   for (int j = 0; j < kPubUnroll; ++j) {
@@ -200,8 +205,10 @@ __global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __gri
       st_u4(ctx_k + ob, oldk);
       st_u4(ctx_v + ob, oldv);
     }
-    st_u4(slot_k + off, kout);
-    st_u4(slot_v + off, vin);
+    if (to_slot) {
+      st_u4(slot_k + off, kout);
+      st_u4(slot_v + off, vin);
+    }
     if (own) {
       const size_t cb = static_cast<size_t>(I.ctx) * upf + off;
       st_u4(ctx_k + cb, kout);

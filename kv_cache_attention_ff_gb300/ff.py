@@ -24,7 +24,7 @@ EXPORTS = [
     "ff_desc_default", "ff_bank_create", "ff_anchor_publish", "ff_render_attn", "ff_bank_destroy",
     "ff_bank_gamma", "ff_bank_slot_info", "ff_bank_bytes", "ff_bank_error_poll", "ff_status_string",
     "ff_plan_chunk", "ff_bank_set_timing", "ff_bank_read_timing", "ff_render_kernel_count",
-    "ff_attention_noalloc", "ff_bank_wait_probe",
+    "ff_attention_noalloc", "ff_bank_wait_probe", "ff_planner_attn", "ff_plan_planner_block",
 ]
 
 
@@ -41,7 +41,8 @@ class BankDesc(ctypes.Structure):
         ("chunk_frames", ctypes.c_int), ("anchor_stride", ctypes.c_int), ("anchor_capacity", ctypes.c_int),
         ("total_frames", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
         ("frame_h", ctypes.c_int), ("frame_w", ctypes.c_int), ("rope_theta", ctypes.c_double),
-        ("max_bytes", ctypes.c_size_t), ("device", ctypes.c_int),
+        ("max_bytes", ctypes.c_size_t), ("device", ctypes.c_int), ("planner_block", ctypes.c_int),
+        ("planner_history", ctypes.c_int),
     ]
 
 
@@ -50,6 +51,13 @@ class ChunkPlan(ctypes.Structure):
         ("first_frame", ctypes.c_int), ("n_frames", ctypes.c_int), ("n_anchors", ctypes.c_int),
         ("anchors", ctypes.c_int * 2), ("n_hist", ctypes.c_int), ("hist_first", ctypes.c_int),
         ("hist_frames", ctypes.c_int), ("slot", ctypes.c_int), ("key_frames", ctypes.c_int),
+    ]
+
+
+class PlannerPlan(ctypes.Structure):
+    _fields_ = [
+        ("first_anchor", ctypes.c_int), ("n_anchors", ctypes.c_int), ("hist_first_block", ctypes.c_int),
+        ("n_hist_blocks", ctypes.c_int), ("hist_frames", ctypes.c_int), ("key_frames", ctypes.c_int),
     ]
 
 
@@ -86,6 +94,8 @@ def _lib():
         lib.ff_render_kernel_count.argtypes = [P, I, ctypes.POINTER(I)]
         lib.ff_attention_noalloc.argtypes = [V, V, V, V, I, I, I, I, V]
         lib.ff_bank_wait_probe.argtypes = [P, I, V]
+        lib.ff_planner_attn.argtypes = [P, I, I, V, V, V, V, V]
+        lib.ff_plan_planner_block.argtypes = [ctypes.POINTER(BankDesc), I, ctypes.POINTER(PlannerPlan)]
         for name in EXPORTS:
             if name != "ff_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -116,6 +126,12 @@ def make_desc(**kw) -> BankDesc:
 def plan_chunk(desc: BankDesc, chunk: int) -> ChunkPlan:
     p = ChunkPlan()
     _check(_lib().ff_plan_chunk(ctypes.byref(desc), chunk, ctypes.byref(p)), "ff_plan_chunk")
+    return p
+
+
+def plan_planner_block(desc: BankDesc, block: int) -> PlannerPlan:
+    p = PlannerPlan()
+    _check(_lib().ff_plan_planner_block(ctypes.byref(desc), block, ctypes.byref(p)), "ff_plan_planner_block")
     return p
 
 
@@ -176,6 +192,13 @@ class Bank:
         _check(_lib().ff_render_attn(self.handle, layer, stage, chunk, _ptr(q_pre, shape, "q_pre"),
                                      _ptr(k_pre, shape, "k_pre"), _ptr(v, shape, "v"), _ptr(out, shape, "out"),
                                      _stream(stream, self.device)), "ff_render_attn")
+
+    def planner_attn(self, layer, block, q_pre, k_pre, v, out, stream=None):
+        n = plan_planner_block(self.desc, block).n_anchors
+        shape = (n * self.T, self.desc.heads, self.desc.head_dim)
+        _check(_lib().ff_planner_attn(self.handle, layer, block, _ptr(q_pre, shape, "q_pre"), _ptr(k_pre, shape, "k_pre"),
+                                      _ptr(v, shape, "v"), _ptr(out, shape, "out"), _stream(stream, self.device)),
+               "ff_planner_attn")
 
     def render_attn_raw(self, layer, stage, chunk, q_ptr, k_ptr, v_ptr, out_ptr, stream_handle) -> int:
         """Pointer-level call (no checks in Python); returns the status code."""

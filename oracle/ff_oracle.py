@@ -150,6 +150,32 @@ def anchor_slot(a: int, stride: int, capacity: int) -> int:
     return (a // stride) % capacity
 
 
+# Planner blocks ([FF-onedev] "무엇과 다른가": the planner produces the clean
+# anchors B_P at a time, history H_P blocks, context budget W_ctx; "어떻게 쓰나":
+# planner blocks attend causally to the clean KV of the previous blocks).
+
+
+def num_anchors(total_frames: int, stride: int) -> int:
+    return (total_frames - 1) // stride + 1
+
+
+def num_planner_blocks(total_frames: int, stride: int, block: int) -> int:
+    return -(-num_anchors(total_frames, stride) // block)
+
+
+def planner_block_anchors(b: int, block: int, stride: int, total_frames: int) -> list[int]:
+    """Anchor frames produced by planner block b."""
+    n = num_anchors(total_frames, stride)
+    if not 0 <= b * block < n:
+        raise ValueError("planner block past the last anchor")
+    return [a * stride for a in range(b * block, min((b + 1) * block, n))]
+
+
+def planner_history_blocks(b: int, history: int) -> list[int]:
+    """Blocks whose clean KV planner block b attends to, oldest first."""
+    return list(range(max(0, b - history), b))
+
+
 # ---------------------------------------------------------------------------
 # Rotary position embedding (reading: the backbone's three-axis RoPE).
 # ---------------------------------------------------------------------------
@@ -452,6 +478,30 @@ class OracleBank:
         sl.k = k_rot_bits
         sl.v = np.array(v_bits, copy=True)
         self.next_chunk[layer][stage] += 1
+
+    def planner_attn(self, layer: int, block: int, q_bits, k_bits, v_bits, planner_block: int = 3,
+                     planner_history: int = 6):
+        """Attention of planner block `block`: its rotated queries over
+        [clean anchor KV of the previous planner_history blocks; the block's own
+        rotated K/V].  Publishes nothing.  Returns (out f64, context frames)."""
+        c = self.cfg
+        ks, vs, frames = [], [], []
+        for hb in planner_history_blocks(block, planner_history):
+            for a in planner_block_anchors(hb, planner_block, c.anchor_stride, c.total_frames):
+                sl = self.anchor[layer][anchor_slot(a, c.anchor_stride, c.anchor_capacity)]
+                if sl.tag != a:
+                    raise OracleError("FF_ERR_ANCHOR_MISSING", f"anchor {a}")
+                ks.append(sl.k)
+                vs.append(sl.v)
+                frames.append(a)
+        own = planner_block_anchors(block, planner_block, c.anchor_stride, c.total_frames)
+        pos = token_positions(own, c.frame_h, c.frame_w)
+        ks.append(rope_k_bits(k_bits, pos, c.head_dim, c.rope_theta))
+        vs.append(np.asarray(v_bits))
+        frames.extend(own)
+        q = rope_q_f64(q_bits, pos, c.head_dim, c.rope_theta)
+        out = attention_f64(q, bf16_bits_to_f64(np.concatenate(ks)), bf16_bits_to_f64(np.concatenate(vs)))
+        return out, frames
 
     def stage_tags(self, layer: int, stage: int) -> list[int]:
         return [sl.tag for sl in self.stage[layer][stage]]

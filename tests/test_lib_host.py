@@ -96,3 +96,24 @@ def test_synth_bf16_rounding_matches_torch():
     assert np.array_equal(synth.f32_to_bf16_bits(x), ref)
     got = synth._bf16_torch(torch.from_numpy(x)).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fields", [
+    dict(total_frames=81, anchor_stride=10, planner_block=3, planner_history=6),
+    dict(total_frames=261, anchor_stride=10, planner_block=3, planner_history=6, anchor_capacity=27),
+    dict(total_frames=13, anchor_stride=4, planner_block=3, planner_history=1, anchor_capacity=4),
+    dict(total_frames=100, anchor_stride=7, planner_block=2, planner_history=3),
+])
+def test_planner_plan_matches_oracle(ff, fields):
+    d = ff.make_desc(**fields)
+    N, S, B, H = fields["total_frames"], fields["anchor_stride"], fields["planner_block"], fields["planner_history"]
+    nb = fo.num_planner_blocks(N, S, B)
+    for b in range(nb):
+        p = ff.plan_planner_block(d, b)
+        own = fo.planner_block_anchors(b, B, S, N)
+        hist = fo.planner_history_blocks(b, H)
+        assert p.first_anchor * S == own[0] and p.n_anchors == len(own)
+        assert p.n_hist_blocks == len(hist) and (not hist or p.hist_first_block == hist[0])
+        assert p.key_frames == len(own) + B * len(hist)
+    with pytest.raises(ff.FFError):
+        ff.plan_planner_block(d, nb)

@@ -203,3 +203,46 @@ def test_tiny_bank_render_equals_bruteforce_over_named_frames():
             bf = np.array(fo.attention_bruteforce(Q.tolist(), K.tolist(), V.tolist()))
             assert np.allclose(res.out, bf, atol=1e-12, rtol=0)
             assert res.key_frames == len(frames_k)
+
+
+def test_planner_blocks_and_w_ctx():
+    # onedev.kr/papers/332 "무엇과 다른가": 9 anchors produced 3 at a time; planner history
+    # H_P = 6 and context budget W_ctx = 21 = 6 * 3 + 3.
+    assert fo.num_planner_blocks(81, 10, 3) == 3
+    assert [fo.planner_block_anchors(b, 3, 10, 81) for b in range(3)] == [[0, 10, 20], [30, 40, 50], [60, 70, 80]]
+    assert fo.num_planner_blocks(261, 10, 3) == 9
+    widths = []
+    for b in range(9):
+        hist = fo.planner_history_blocks(b, 6)
+        frames = [a for hb in hist for a in fo.planner_block_anchors(hb, 3, 10, 261)]
+        frames += fo.planner_block_anchors(b, 3, 10, 261)
+        widths.append(len(frames))
+        if b == 8:
+            assert frames == list(range(60, 261, 10))
+    assert max(widths) == 21 and widths == [3, 6, 9, 12, 15, 18, 21, 21, 21]
+    # 13 latents at stride 4: anchors {0,4,8,12}, blocks {0,4,8} and {12}
+    assert [fo.planner_block_anchors(b, 3, 4, 13) for b in range(2)] == [[0, 4, 8], [12]]
+    with pytest.raises(ValueError):
+        fo.planner_block_anchors(2, 3, 4, 13)
+
+
+def test_planner_attention_equals_bruteforce_over_named_frames():
+    cfg = _tiny_cfg(heads=2, head_dim=12, frame_h=1, frame_w=2, total_frames=13, anchor_stride=4, anchor_capacity=4)
+    T = cfg.tokens_per_frame
+    rng = np.random.default_rng(31)
+    bits = lambda n: fo.f64_to_bf16_bits(rng.standard_normal((n * T, cfg.heads, cfg.head_dim)))
+    bank = fo.OracleBank(cfg)
+    ak, av = bits(3), bits(3)
+    bank.anchor_publish(0, 0, 3, ak, av)          # clean KV of block 0 = anchors 0, 4, 8
+    q, k, v = bits(1), bits(1), bits(1)           # block 1 = anchor 12
+    out, frames = bank.planner_attn(0, 1, q, k, v, planner_block=3, planner_history=6)
+    assert frames == [0, 4, 8, 12]
+    Ks = [fo.rope_k_bits(ak[j * T:(j + 1) * T], fo.token_positions([4 * j], 1, 2), 12, 1e4) for j in range(3)]
+    Ks.append(fo.rope_k_bits(k, fo.token_positions([12], 1, 2), 12, 1e4))
+    K = fo.bf16_bits_to_f64(np.concatenate(Ks))
+    V = fo.bf16_bits_to_f64(np.concatenate([av, v]))
+    Q = fo.rope_q_f64(q, fo.token_positions([12], 1, 2), 12, 1e4)
+    bf = np.array(fo.attention_bruteforce(Q.tolist(), K.tolist(), V.tolist()))
+    assert np.allclose(out, bf, atol=1e-12, rtol=0)
+    with pytest.raises(fo.OracleError):
+        fo.OracleBank(cfg).planner_attn(0, 1, q, k, v, planner_block=3, planner_history=6)
