@@ -279,6 +279,7 @@ def run_gpu(args):
     e2e = None if args.no_e2e else run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
 
     planner = None if args.no_e2e else run_planner(stream, args, dev)
+    packed = None if args.no_e2e else run_packed(stream, args, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -298,7 +299,7 @@ def run_gpu(args):
             "kernel_ms": {"publish_gather": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "packed": packed, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -342,6 +343,45 @@ def run_planner(stream, args, dev):
     flops = 4.0 * 4680 * 21 * T * D * H
     return {"workload": "planner block, 1.3B 480p shape, 21 context frames (W_ctx)", "queries": 4680,
             "keys": 21 * T, "ms_per_call": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+
+
+def run_packed(stream, args, dev):
+    """Packed block-causal renderer forward of one stage of the 81-latent 1.3B 480p
+    clip: 27 chunks of 4680 queries over 5..20 key frames each, one call."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff, synth
+    T, H, D, N = 1560, 12, 128, 81
+    pb = ff.Bank(n_layers=1, n_stages=1, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                 total_frames=N, heads=H, head_dim=D, frame_h=30, frame_w=52, planner_history=0, device=dev.index)
+    with torch.cuda.stream(stream):
+        q, k = (synth.device_frames(2, 0, 0, t, list(range(N)), T, H, D, "ar", device=dev) for t in (0, 1))
+        v = synth.device_frames(2, 0, 0, 2, list(range(N)), T, H, D, "normal", device=dev)
+        ak = synth.device_frames(2, 0, synth.ANCHOR_STREAM, synth.K, list(range(0, 81, 10)), T, H, D, "ar", device=dev)
+        av = synth.device_frames(2, 0, synth.ANCHOR_STREAM, synth.V, list(range(0, 81, 10)), T, H, D, "normal",
+                                 device=dev)
+        ws = torch.empty(pb.packed_workspace_bytes(), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+    torch.cuda.synchronize()
+    reps = max(3, args.steps // 4)
+    for _ in range(2):
+        pb.packed_render_attn(q, k, v, ak, av, out, ws, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        pb.packed_render_attn(q, k, v, ak, av, out, ws, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    assert pb.error_poll() == 0
+    pb.close()
+    key_frames = sum(min(20, 5 + 3 * i) for i in range(27))  # 495
+    flops = 4.0 * (3 * T) * (key_frames * T) * D * H
+    return {"workload": "packed block-causal forward, one stage of the 81-latent 1.3B 480p clip",
+            "chunks": 27, "key_frames_total": key_frames, "ms_per_call": round(ms, 3),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
 
 
 def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):

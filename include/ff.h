@@ -131,6 +131,25 @@ int ff_render_attn(ff_bank_t* bank, int layer, int stage, int chunk,
 int ff_planner_attn(ff_bank_t* bank, int layer, int block, const void* q_pre, const void* k_pre, const void* v,
                     void* out, void* stream);
 
+/* Packed block-causal renderer forward of one denoising stage: every chunk of
+ * the video in one call (onedev.kr/papers/332, "어떻게 쓰나": in training the
+ * renderer runs as a block-causal forward rather than chunk-by-chunk cache
+ * updates; its targets attend to the Gamma(i) clean anchor KV and the previous
+ * H same-noise-level chunks).  Rows of chunk i attend to [Gamma(i) anchors;
+ * chunks max(0, i-H) .. i-1; chunk i], exactly the key set ff_render_attn uses
+ * for chunk i when the chunks are rendered in order at one stage.
+ * q_pre, k_pre, v: device bf16 [N * T, heads, head_dim] for all N latent frames,
+ * before rotary encoding; anchor_k_pre, anchor_v: [A * T, heads, head_dim] for
+ * the A anchors 0, Delta, 2 Delta, ...; out: [N * T, heads, head_dim].
+ * workspace: device buffer of at least ff_packed_workspace_bytes bytes, owned by
+ * the caller (rotated K, V of anchors and frames and rotated Q).  Uses the bank's
+ * description and rotary tables only: no bank state is read or changed.
+ * Errors: FF_ERR_ARG for null/misaligned pointers or a short workspace. */
+int ff_packed_workspace_bytes(const ff_bank_t* bank, size_t* bytes);
+int ff_packed_render_attn(ff_bank_t* bank, const void* q_pre, const void* k_pre, const void* v,
+                          const void* anchor_k_pre, const void* anchor_v, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Wait for all work the bank enqueued, then free everything.  NULL-safe. */
 int ff_bank_destroy(ff_bank_t* bank);
 

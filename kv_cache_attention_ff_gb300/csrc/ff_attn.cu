@@ -57,16 +57,58 @@ struct AttnCfg {
 
 constexpr int kAttnThreads = 320;
 
-template <int D>
-__device__ __forceinline__ void piece_coords(const AttnParams& p, int piece, int& head, int& qb, int& kv0, int& kv1) {
+// Piece -> (head, group, query block of the group, key-tile range).
+struct Piece {
+  int head, g, qb, kv0, kv1;
+};
+
+__device__ __forceinline__ Piece decode_piece(const AttnParams& p, int piece) {
+  Piece r;
   const int per_head = p.n_split * p.n_qb;
-  head = piece / per_head;
-  const int rem = piece - head * per_head;
+  r.head = piece / per_head;
+  const int rem = piece - r.head * per_head;
   const int split = rem / p.n_qb;
-  qb = rem - split * p.n_qb;
-  kv0 = static_cast<int>((static_cast<long long>(split) * p.n_kv) / p.n_split);
-  kv1 = static_cast<int>((static_cast<long long>(split + 1) * p.n_kv) / p.n_split);
+  const int lin = rem - split * p.n_qb;
+  int g = 0;
+  while (g + 1 < p.n_groups && p.groups[g + 1].qb0 <= lin) ++g;
+  r.g = g;
+  r.qb = lin - p.groups[g].qb0;
+  const int nkv = p.groups[g].n_kv;
+  r.kv0 = static_cast<int>((static_cast<long long>(split) * nkv) / p.n_split);
+  r.kv1 = static_cast<int>((static_cast<long long>(split + 1) * nkv) / p.n_split);
+  return r;
 }
+
+// Walks the key tiles of a group in order: for each tile its first key row and
+// the number of valid keys (<= 128; the rest of the tile belongs to another
+// segment or lies past the buffer).  Segment fields are reloaded only when a
+// segment ends.
+struct TileCursor {
+  int s, tw, row0, rows, end_tile;
+
+  __device__ __forceinline__ void load(const AttnGroup& G) {
+    row0 = G.seg_row0[s];
+    rows = G.seg_rows[s];
+    end_tile = (s + 1 < G.n_seg) ? G.seg_tile0[s + 1] : G.n_kv;
+  }
+  __device__ __forceinline__ void start(const AttnGroup& G, int t) {
+    s = 0;
+    while (s + 1 < G.n_seg && G.seg_tile0[s + 1] <= t) ++s;
+    tw = t - G.seg_tile0[s];
+    load(G);
+  }
+  // tile t must follow the previous call's tile
+  __device__ __forceinline__ void next(const AttnGroup& G, int t, int& row, int& valid) {
+    if (t == end_tile) {
+      ++s;
+      tw = 0;
+      load(G);
+    }
+    row = row0 + tw * 128;
+    valid = min(128, rows - tw * 128);
+    ++tw;
+  }
+};
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -135,15 +177,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int seg = 0;
       bool ok = true;
       for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x, ++seg) {
-        int head, qb, kv0, kv1;
-        piece_coords<D>(p, piece, head, qb, kv0, kv1);
+        const Piece pc = decode_piece(p, piece);
+        const AttnGroup& G = p.groups[pc.g];
+        const int head = pc.head, kv0 = pc.kv0, kv1 = pc.kv1;
         if (seg > 0 && !(ok = mbar_wait(q_empty, (seg - 1) & 1, abort_flag, err))) break;
         mbar_expect_tx(q_full, 2 * C::Q_BYTES);
         for (int t = 0; t < 2; ++t)
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(sQ + t * C::Q_BYTES + kb * C::BLK, &tmQ, head * D + kb * 64, qb * 256 + t * 128, q_full);
+            tma_load_2d(sQ + t * C::Q_BYTES + kb * C::BLK, &tmQ, head * D + kb * 64,
+                        G.q_row0 + pc.qb * 256 + t * 128, q_full);
         const int n = kv1 - kv0;
         // consumption order: K_0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}
+        TileCursor kc, vc;
+        kc.start(G, kv0);
+        vc.start(G, kv0);
         for (int step = 0; step <= n && ok; ++step) {
           for (int which = 0; which < 2; ++which) {
             const bool is_k = (which == 0);
@@ -155,9 +202,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (use > 0 && !(ok = mbar_wait(kv_empty + stage, (use - 1) & 1, abort_flag, err))) break;
             mbar_expect_tx(kv_full + stage, C::KV_BYTES);
             const CUtensorMap* map = is_k ? &tmK : &tmV;
+            int krow, kvalid;
+            (is_k ? kc : vc).next(G, kv0 + j, krow, kvalid);
             for (int kb = 0; kb < C::KB; ++kb)
-              tma_load_2d(sKV + stage * C::KV_BYTES + kb * C::BLK, map, head * D + kb * 64, (kv0 + j) * 128,
-                          kv_full + stage);
+              tma_load_2d(sKV + stage * C::KV_BYTES + kb * C::BLK, map, head * D + kb * 64, krow, kv_full + stage);
             ++n_load;
           }
         }
@@ -198,9 +246,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
 
       for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x, ++seg) {
-        int head, qb, kv0, kv1;
-        piece_coords<D>(p, piece, head, qb, kv0, kv1);
-        const int n = kv1 - kv0;
+        const Piece pc = decode_piece(p, piece);
+        const int n = pc.kv1 - pc.kv0;
         if (!(ok = mbar_wait(q_full, seg & 1, abort_flag, err))) break;
         tc_fence_after();
         for (int j = 0; j < n && ok; ++j) {
@@ -244,10 +291,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t n_sf = 0, n_od = 0;
     bool ok = true;
     for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x) {
-      int head, qb, kv0, kv1;
-      piece_coords<D>(p, piece, head, qb, kv0, kv1);
-      const int n = kv1 - kv0;
+      const Piece pc = decode_piece(p, piece);
+      const AttnGroup& G = p.groups[pc.g];
+      const int head = pc.head, kv0 = pc.kv0;
+      const int n = pc.kv1 - pc.kv0;
       float m_run = -INFINITY, l_run = 0.f;
+      TileCursor cur;
+      cur.start(G, kv0);
       for (int j = 0; j < n; ++j) {
         if (!(ok = mbar_wait(s_full + t, n_sf & 1, abort_flag, err))) break;
         ++n_sf;
@@ -260,9 +310,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(s_free + t);
-        const int tile = kv0 + j;
-        if (tile == p.n_kv - 1) {
-          const int valid = p.nk - tile * 128;
+        int krow, valid;
+        cur.next(G, kv0 + j, krow, valid);
+        if (valid < 128) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = -INFINITY;
@@ -318,16 +368,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!(ok = mbar_wait(o_done + t, n_od & 1, abort_flag, err))) break;
       ++n_od;
       tc_fence_after();
-      const int row = qb * 256 + t * 128 + r;
+      const int lrow = pc.qb * 256 + t * 128 + r;  // row within the group
       if (p.n_split == 1) {
         const float inv = 1.0f / l_run;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(row) * p.heads + head) * D;
+        __nv_bfloat16* dst =
+            static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(G.q_row0 + lrow) * p.heads + head) * D;
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
           float o[32];
           tmem_ld32(tO + cc, o);
           tmem_wait_ld();
-          if (row < p.nq) {
+          if (lrow < G.nq) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -370,17 +421,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 8;  // elements per thread
-  const int unit = blockIdx.x;  // head * n_qb + qb
+  const int unit = blockIdx.x;  // head * n_qb + linear query block
   const int head = unit / p.n_qb;
-  const int qb = unit - head * p.n_qb;
+  const int lin = unit - head * p.n_qb;
+  int g = 0;
+  while (g + 1 < p.n_groups && p.groups[g + 1].qb0 <= lin) ++g;
+  const AttnGroup& G = p.groups[g];
+  const int qb = lin - G.qb0;
   const int rloc = blockIdx.y * 32 + (threadIdx.x >> 3);  // 0..255
   const int part = threadIdx.x & 7;
-  const int row = qb * 256 + rloc;
-  if (row >= p.nq) return;
+  const int lrow = qb * 256 + rloc;
+  if (lrow >= G.nq) return;
+  const int row = G.q_row0 + lrow;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   float m = -INFINITY;
   for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + qb;
+    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + lin;
     m = fmaxf(m, ml[piece * 256 + rloc].x);
   }
   float acc[PER];
@@ -388,7 +444,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f;
   for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + qb;
+    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + lin;
     const float2 v = ml[piece * 256 + rloc];
     const float w = exp2f(v.x - m);
     l = __fmaf_rn(v.y, w, l);

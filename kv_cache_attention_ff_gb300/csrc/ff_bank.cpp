@@ -718,12 +718,9 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   AttnParams ap{};
   ap.out = out;
   ap.err = b->err;
-  ap.nq = nq;
-  ap.nk = nk;
   ap.heads = d.heads;
-  ap.n_qb = (nq + kQBlock - 1) / kQBlock;
-  ap.n_kv = (nk + kKTile - 1) / kKTile;
-  ap.n_split = choose_split(d.heads * ap.n_qb, ap.n_kv, b->sm_count);
+  attn_single_group(ap, nq, nk);
+  ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
   if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->max_pieces) ap.n_split = 1;
   ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
   ap.part_o = sc.part_o;
@@ -841,12 +838,9 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
   AttnParams ap{};
   ap.out = out;
   ap.err = b->err;
-  ap.nq = nq;
-  ap.nk = nk;
   ap.heads = d.heads;
-  ap.n_qb = (nq + kQBlock - 1) / kQBlock;
-  ap.n_kv = (nk + kKTile - 1) / kKTile;
-  ap.n_split = choose_split(d.heads * ap.n_qb, ap.n_kv, b->sm_count);
+  attn_single_group(ap, nq, nk);
+  ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
   if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->planner_max_pieces) ap.n_split = 1;
   ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
   ap.part_o = sc.part_o;
@@ -869,6 +863,127 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
   cudaEventRecord(b->ev_planner, s);
   b->planner_stream = s;
   b->planner_used = true;
+  return FF_OK;
+}
+
+int ff_packed_workspace_bytes(const ff_bank_t* b, size_t* bytes) {
+  if (!b || !bytes) return FF_ERR_ARG;
+  const size_t frames = static_cast<size_t>(n_anchor_frames(b->d)) + b->d.total_frames;
+  *bytes = (2 * frames + b->d.total_frames) * b->frame_bytes;
+  return FF_OK;
+}
+
+int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, const void* v, const void* anchor_k_pre,
+                          const void* anchor_v, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!b || !q_pre || !k_pre || !v || !anchor_k_pre || !anchor_v || !out || !workspace || !aligned16(q_pre) ||
+      !aligned16(k_pre) || !aligned16(v) || !aligned16(anchor_k_pre) || !aligned16(anchor_v) || !aligned16(out) ||
+      !aligned16(workspace))
+    return FF_ERR_ARG;
+  const ff_bank_desc& d = b->d;
+  size_t need = 0;
+  ff_packed_workspace_bytes(b, &need);
+  if (workspace_bytes < need) return FF_ERR_ARG;
+  const int A = n_anchor_frames(d);
+  const int N = d.total_frames;
+  const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
+  if ((A + N) * T > (1ll << 30)) return FF_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* kall = ws;                                          // [A + N frames]: anchors, then frames
+  uint8_t* vall = ws + static_cast<size_t>(A + N) * b->frame_bytes;
+  uint8_t* qrot = ws + 2 * static_cast<size_t>(A + N) * b->frame_bytes;  // [N frames]
+
+  // 1. rotary encoding of every anchor and frame into the workspace (batches of kMaxItems frames)
+  G1Params prm{};
+  prm.rope64 = b->rope64;
+  prm.rope32 = b->rope32;
+  prm.y_base = b->rope_y_base;
+  prm.x_base = b->rope_x_base;
+  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
+  prm.units_per_row = d.heads * d.head_dim / 8;
+  prm.units_per_head = d.head_dim / 8;
+  prm.frame_w = d.frame_w;
+  prm.pt = b->pt;
+  prm.py = b->py;
+  prm.px = b->px;
+  prm.ctx_k = kall;
+  prm.ctx_v = vall;
+  int rc;
+  for (int f0 = 0; f0 < A + N; f0 += kMaxItems) {
+    const int f1 = std::min(A + N, f0 + kMaxItems);
+    // frames (not anchors) of this batch start at input frame max(f0, A) - A
+    const int first_frame = std::max(f0, A) - A;
+    prm.q_in = static_cast<const uint8_t*>(q_pre) + static_cast<size_t>(first_frame) * b->frame_bytes;
+    prm.k_in = static_cast<const uint8_t*>(k_pre) + static_cast<size_t>(first_frame) * b->frame_bytes;
+    prm.v_in = static_cast<const uint8_t*>(v) + static_cast<size_t>(first_frame) * b->frame_bytes;
+    prm.q_rot = qrot + static_cast<size_t>(first_frame) * b->frame_bytes;
+    int n_items = 0;
+    for (int f = f0; f < f1; ++f) {
+      G1Item& it = prm.items[n_items++];
+      it.ctx = f;
+      it.old_ctx = -1;
+      if (f < A) {
+        it.kind = kItemRotCtx;
+        it.k = static_cast<const uint8_t*>(anchor_k_pre) + static_cast<size_t>(f) * b->frame_bytes;
+        it.v = static_cast<const uint8_t*>(anchor_v) + static_cast<size_t>(f) * b->frame_bytes;
+        it.r = 0;
+        it.t = f * d.anchor_stride;
+      } else {
+        it.kind = kItemOwnCtx;
+        it.k = it.v = nullptr;
+        it.r = (f - A) - first_frame;
+        it.t = f - A;
+      }
+    }
+    prm.n_items = n_items;
+    if ((rc = cuda_err(launch_publish(prm, 0, s), "packed rope launch")) != FF_OK) return rc;
+  }
+
+  // 2. block-causal attention: one query group per chunk, up to three key segments
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(b, &tq, qrot, static_cast<int>(N * T))) != FF_OK) return rc;
+  if ((rc = make_map(b, &tk, kall, static_cast<int>((A + N) * T))) != FF_OK) return rc;
+  if ((rc = make_map(b, &tv, vall, static_cast<int>((A + N) * T))) != FF_OK) return rc;
+  const int nc = n_chunks(d);
+  for (int c0 = 0; c0 < nc; c0 += kMaxGroups) {
+    const int c1 = std::min(nc, c0 + kMaxGroups);
+    AttnParams ap{};
+    ap.out = out;
+    ap.err = b->err;
+    ap.heads = d.heads;
+    ap.n_split = 1;
+    ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
+    ap.n_groups = c1 - c0;
+    int qb = 0;
+    for (int i = c0; i < c1; ++i) {
+      ff_chunk_plan pl;
+      plan(d, i, &pl);
+      AttnGroup& g = ap.groups[i - c0];
+      g.q_row0 = static_cast<int>(pl.first_frame * T);
+      g.nq = static_cast<int>(pl.n_frames * T);
+      g.qb0 = qb;
+      qb += (g.nq + kQBlock - 1) / kQBlock;
+      g.n_seg = 0;
+      int tiles = 0;
+      auto add = [&](long long row0, long long rows) {
+        g.seg_row0[g.n_seg] = static_cast<int>(row0);
+        g.seg_rows[g.n_seg] = static_cast<int>(rows);
+        g.seg_tile0[g.n_seg] = tiles;
+        tiles += static_cast<int>((rows + kKTile - 1) / kKTile);
+        ++g.n_seg;
+      };
+      for (int j = 0; j < pl.n_anchors; ++j) add((pl.anchors[j] / d.anchor_stride) * T, T);
+      const int hist_first_frame = d.chunk_frames * pl.hist_first;
+      add((A + hist_first_frame) * T, (pl.hist_frames + pl.n_frames) * T);
+      g.n_kv = tiles;
+    }
+    ap.n_qb = qb;
+    ap.n_pieces = d.heads * ap.n_qb;
+    const int grid = std::min(ap.n_pieces, b->sm_count);
+    if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "packed attention launch")) != FF_OK)
+      return rc;
+  }
   return FF_OK;
 }
 

@@ -18,7 +18,8 @@ enum ItemKind : int {
   kItemCopy = 0,    // context frame <- (k, v) source frame (anchor or history slot)
   kItemOwn = 1,     // own chunk frame r: RoPE(q) -> q_rot, RoPE(k) and v -> slot frame r and context
   kItemAnchor = 2,  // anchor input frame r: RoPE(k) and v -> anchor slot
-  kItemOwnCtx = 3,  // like kItemOwn but nothing is published (planner blocks)
+  kItemOwnCtx = 3,  // like kItemOwn but nothing is published (planner blocks, packed frames)
+  kItemRotCtx = 4,  // context frame <- (RoPE(k), v) of the source frame in (k, v); no Q, nothing published
 };
 
 struct G1Item {
@@ -57,18 +58,53 @@ struct G1Params {
 
 // ----------------------------------------------------------------- attention
 
+// Attention work is described as query groups, each a run of query rows with
+// its own list of key segments (row ranges of the K/V buffers).  A renderer or
+// planner call is one group with one segment (the gathered context); a packed
+// block-causal forward has one group per chunk with up to three segments
+// (left anchor, right anchor, history + own chunk).
+constexpr int kMaxGroups = 96;
+constexpr int kMaxSegs = 3;
+
+struct AttnGroup {
+  int q_row0;              // first query row of the group
+  int nq;                  // query rows
+  int qb0;                 // first linear 256-row query block of the group
+  int n_seg;               // key segments (1..kMaxSegs)
+  int seg_row0[kMaxSegs];  // first key row of each segment
+  int seg_rows[kMaxSegs];  // key rows of each segment
+  int seg_tile0[kMaxSegs]; // first 128-key tile of each segment in the group's tile sequence
+  int n_kv;                // tiles over all segments
+};
+
 struct AttnParams {
-  void* out;            // bf16 [Nq, h, d]
+  void* out;            // bf16 [query rows, h, d]
   float* part_o;        // [pieces][256][d] unnormalised partial outputs (split only)
   float* part_ml;       // [pieces][256][2] running max (log2 units) and sum
   unsigned int* err;    // device error word
-  int nq, nk, heads;
-  int n_qb;             // 256-row query blocks
-  int n_kv;             // 128-key tiles
+  int heads;
+  int n_qb;             // linear 256-row query blocks over all groups
   int n_split;          // key-range splits per query block
   int n_pieces;         // heads * n_split * n_qb
   float scale_log2;     // log2(e) / sqrt(d)
+  int n_groups;
+  AttnGroup groups[kMaxGroups];
 };
+
+// Fill `p` with the single group [0, nq) x one key segment [0, nk).
+inline void attn_single_group(AttnParams& p, int nq, int nk) {
+  p.n_groups = 1;
+  AttnGroup& g = p.groups[0];
+  g.q_row0 = 0;
+  g.nq = nq;
+  g.qb0 = 0;
+  g.n_seg = 1;
+  g.seg_row0[0] = 0;
+  g.seg_rows[0] = nk;
+  g.seg_tile0[0] = 0;
+  g.n_kv = (nk + 127) / 128;
+  p.n_qb = (nq + 255) / 256;
+}
 
 // Host launchers (ff_publish.cu / ff_attn.cu).
 cudaError_t launch_publish(const G1Params& p, int grid, cudaStream_t s);

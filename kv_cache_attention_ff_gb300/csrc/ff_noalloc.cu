@@ -124,12 +124,9 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
 
   ff::AttnParams ap{};
   ap.out = out;
-  ap.nq = nq;
-  ap.nk = nk;
   ap.heads = heads;
-  ap.n_qb = n_qb;
-  ap.n_kv = static_cast<int>(n_kv);
-  ap.n_split = split_for(heads * n_qb, ap.n_kv, sms);
+  ff::attn_single_group(ap, nq, nk);
+  ap.n_split = split_for(heads * n_qb, ap.groups[0].n_kv, sms);
   ap.n_pieces = heads * n_qb * ap.n_split;
   const size_t part_rows = static_cast<size_t>(ap.n_pieces) * 256;
   const size_t need = kErrBytes + part_rows * static_cast<size_t>(head_dim) * 4 + part_rows * 8;

@@ -158,17 +158,20 @@ __global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __gri
     return;
   }
 
-  // Own-chunk frame, planner-block frame or anchor frame.
+  // Own-chunk frame, planner-block or packed frame, anchor frame, or a rotated copy.
   const bool own = (kind == kItemOwn) || (kind == kItemOwnCtx);
-  const bool to_slot = (kind != kItemOwnCtx);
+  const bool rot_copy = (kind == kItemRotCtx);
+  const bool to_slot = (kind == kItemOwn) || (kind == kItemAnchor);
   const bool save_old = (kind == kItemOwn) && I.old_ctx >= 0;
   const size_t in_base = static_cast<size_t>(I.r) * upf;
+  const uint4* src_k = rot_copy ? slot_k : k_in + in_base;
+  const uint4* src_v = rot_copy ? slot_v : v_in + in_base;
 #pragma unroll
   for (int j = 0; j < kPubUnroll; ++j) {
     const int off = base + j * kPubThreads;
     if (off >= upf) break;
-    const uint4 kin = ld_stream(k_in + in_base + off);
-    const uint4 vin = ld_stream(v_in + in_base + off);
+    const uint4 kin = ld_stream(src_k + off);
+    const uint4 vin = ld_stream(src_v + off);
     uint4 qin = make_uint4(0, 0, 0, 0);
     if (own) qin = ld_stream(q_in + in_base + off);
     uint4 oldk = make_uint4(0, 0, 0, 0), oldv = make_uint4(0, 0, 0, 0);
@@ -209,12 +212,12 @@ __global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __gri
       st_u4(slot_k + off, kout);
       st_u4(slot_v + off, vin);
     }
-    if (own) {
+    if (own || rot_copy) {
       const size_t cb = static_cast<size_t>(I.ctx) * upf + off;
       st_u4(ctx_k + cb, kout);
       st_u4(ctx_v + cb, vin);
-      st_u4(static_cast<uint4*>(p.q_rot) + in_base + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
     }
+    if (own) st_u4(static_cast<uint4*>(p.q_rot) + in_base + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
   }
 }
 

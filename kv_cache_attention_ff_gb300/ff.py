@@ -25,6 +25,7 @@ EXPORTS = [
     "ff_bank_gamma", "ff_bank_slot_info", "ff_bank_bytes", "ff_bank_error_poll", "ff_status_string",
     "ff_plan_chunk", "ff_bank_set_timing", "ff_bank_read_timing", "ff_render_kernel_count",
     "ff_attention_noalloc", "ff_bank_wait_probe", "ff_planner_attn", "ff_plan_planner_block",
+    "ff_packed_workspace_bytes", "ff_packed_render_attn",
 ]
 
 
@@ -95,6 +96,8 @@ def _lib():
         lib.ff_attention_noalloc.argtypes = [V, V, V, V, I, I, I, I, V]
         lib.ff_bank_wait_probe.argtypes = [P, I, V]
         lib.ff_planner_attn.argtypes = [P, I, I, V, V, V, V, V]
+        lib.ff_packed_workspace_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ff_packed_render_attn.argtypes = [P, V, V, V, V, V, V, V, ctypes.c_size_t, V]
         lib.ff_plan_planner_block.argtypes = [ctypes.POINTER(BankDesc), I, ctypes.POINTER(PlannerPlan)]
         for name in EXPORTS:
             if name != "ff_status_string":
@@ -199,6 +202,25 @@ class Bank:
         _check(_lib().ff_planner_attn(self.handle, layer, block, _ptr(q_pre, shape, "q_pre"), _ptr(k_pre, shape, "k_pre"),
                                       _ptr(v, shape, "v"), _ptr(out, shape, "out"), _stream(stream, self.device)),
                "ff_planner_attn")
+
+    def packed_workspace_bytes(self) -> int:
+        n = ctypes.c_size_t()
+        _check(_lib().ff_packed_workspace_bytes(self.handle, ctypes.byref(n)), "ff_packed_workspace_bytes")
+        return n.value
+
+    def packed_render_attn(self, q_pre, k_pre, v, anchor_k_pre, anchor_v, out, workspace, stream=None):
+        """All chunks of one stage in one block-causal call; `workspace` is a
+        device uint8 tensor of at least packed_workspace_bytes()."""
+        d = self.desc
+        shape = (d.total_frames * self.T, d.heads, d.head_dim)
+        ashape = (((d.total_frames - 1) // d.anchor_stride + 1) * self.T, d.heads, d.head_dim)
+        if not workspace.is_cuda or workspace.numel() * workspace.element_size() < self.packed_workspace_bytes():
+            raise ValueError("workspace too small")
+        _check(_lib().ff_packed_render_attn(
+            self.handle, _ptr(q_pre, shape, "q_pre"), _ptr(k_pre, shape, "k_pre"), _ptr(v, shape, "v"),
+            _ptr(anchor_k_pre, ashape, "anchor_k_pre"), _ptr(anchor_v, ashape, "anchor_v"), _ptr(out, shape, "out"),
+            ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+            _stream(stream, self.device)), "ff_packed_render_attn")
 
     def render_attn_raw(self, layer, stage, chunk, q_ptr, k_ptr, v_ptr, out_ptr, stream_handle) -> int:
         """Pointer-level call (no checks in Python); returns the status code."""

@@ -297,6 +297,25 @@ def attention_rows_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.nda
     return attention_f64(q[rows][:, heads], k[:, heads], v[:, heads])
 
 
+def packed_block_causal(cfg: "BankConfig", q_bits, k_bits, v_bits, anchor_k_bits, anchor_v_bits) -> np.ndarray:
+    """Packed block-causal renderer forward of one stage ([FF-onedev] "어떻게 쓰나":
+    the renderer as one block-causal forward, targets attending to Gamma(i)
+    anchors and the previous H same-noise chunks): by definition the outputs of
+    rendering chunks 0, 1, ... in order at that stage with every anchor resident.
+    Inputs cover all frames ([N*T, h, d]) and all anchors ([A*T, h, d])."""
+    c = cfg
+    T = c.tokens_per_frame
+    bank = OracleBank(BankConfig(**{**c.__dict__, "n_layers": 1, "n_stages": 1,
+                                    "anchor_capacity": num_anchors(c.total_frames, c.anchor_stride)}))
+    bank.anchor_publish(0, 0, num_anchors(c.total_frames, c.anchor_stride), anchor_k_bits, anchor_v_bits)
+    outs = []
+    for i in range(num_chunks(c.total_frames, c.chunk_frames)):
+        s, e = chunk_span(i, c.chunk_frames, c.total_frames)
+        sl = slice(s * T, (e + 1) * T)
+        outs.append(bank.render(0, 0, i, q_bits[sl], k_bits[sl], v_bits[sl]).out)
+    return np.concatenate(outs)
+
+
 def attention_bruteforce(q, k, v, scale=None):
     """Pure-Python triple loop of the same definition (tiny inputs only)."""
     nq, h, d = len(q), len(q[0]), len(q[0][0])

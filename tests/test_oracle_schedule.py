@@ -246,3 +246,36 @@ def test_planner_attention_equals_bruteforce_over_named_frames():
     assert np.allclose(out, bf, atol=1e-12, rtol=0)
     with pytest.raises(fo.OracleError):
         fo.OracleBank(cfg).planner_attn(0, 1, q, k, v, planner_block=3, planner_history=6)
+
+
+def test_packed_block_causal_equals_masked_attention_bruteforce():
+    # The packed forward is the sequential renderer at one stage; check it against a
+    # brute-force attention over all packed tokens with the block mask written out
+    # (chunk i sees anchors Gamma(i), chunks i-H..i-1 and itself).
+    cfg = _tiny_cfg(heads=1, head_dim=12, frame_h=1, frame_w=2, total_frames=13, anchor_stride=4, anchor_capacity=4)
+    T, N, H = cfg.tokens_per_frame, 13, cfg.history
+    rng = np.random.default_rng(41)
+    bits = lambda n: fo.f64_to_bf16_bits(rng.standard_normal((n * T, 1, 12)))
+    q, k, v = bits(N), bits(N), bits(N)
+    ak, av = bits(4), bits(4)
+    got = fo.packed_block_causal(cfg, q, k, v, ak, av)
+    # all keys: anchors (rotated at their frames) then frames (rotated at theirs)
+    Ka = np.concatenate([fo.rope_k_bits(ak[j * T:(j + 1) * T], fo.token_positions([4 * j], 1, 2), 12, 1e4)
+                         for j in range(4)])
+    Kf = fo.rope_k_bits(k, fo.token_positions(list(range(N)), 1, 2), 12, 1e4)
+    K = fo.bf16_bits_to_f64(np.concatenate([Ka, Kf]))[:, 0]
+    V = fo.bf16_bits_to_f64(np.concatenate([av, v]))[:, 0]
+    Q = fo.rope_q_f64(q, fo.token_positions(list(range(N)), 1, 2), 12, 1e4)[:, 0]
+    key_frame = [4 * j for j in range(4) for _ in range(T)] + [f for f in range(N) for _ in range(T)]
+    is_anchor = [True] * (4 * T) + [False] * (N * T)
+    for row in range(N * T):
+        f = row // T
+        i = f // 3
+        s, e = fo.chunk_span(i, 3, N)
+        g = fo.gamma(i, 3, 4, N)
+        lo = 3 * max(0, i - H)
+        allowed = [j for j in range(len(key_frame))
+                   if (is_anchor[j] and key_frame[j] in g) or (not is_anchor[j] and lo <= key_frame[j] <= e)]
+        ref = fo.attention_bruteforce([[Q[row].tolist()]], [[K[j].tolist()] for j in allowed],
+                                      [[V[j].tolist()] for j in allowed])
+        assert np.allclose(got[row, 0], ref[0][0], atol=1e-12)
