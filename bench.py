@@ -224,11 +224,18 @@ def run_gpu(args):
     assert all(c >= 5 for _, _, c in seq)
     kernels_per_call = bank.kernel_count(10)
 
+    # one CUDA stream per denoising stage: calls of different stages are independent
+    # (anti-diagonal chunks of the stage wavefront), so one stage's HBM-bound
+    # publish/gather and combine can run under another stage's attention
+    n_streams = max(1, min(4, args.stage_streams))
+    sstreams = [torch.cuda.Stream(device=dev) for _ in range(n_streams)] if n_streams > 1 else [stream]
+    souts = [torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+
     def call(j):
         layer, st, c = seq[j]
         q, k, v = pool[st][j % 4]
-        rc = bank.render_attn_raw(layer, st, c, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                  stream.cuda_stream)
+        rc = bank.render_attn_raw(layer, st, c, q.data_ptr(), k.data_ptr(), v.data_ptr(), souts[st].data_ptr(),
+                                  sstreams[st % n_streams].cuda_stream)
         if rc != 0:
             raise RuntimeError(f"ff_render_attn failed with status {rc}")
 
@@ -245,8 +252,14 @@ def run_gpu(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    for ss in sstreams:
+        ss.wait_event(e0)
     for j in range(args.warmup, total_calls):
         call(j)
+    for ss in sstreams:
+        done = torch.cuda.Event()
+        done.record(ss)
+        stream.wait_event(done)
     e1.record(stream)
     torch.cuda.synchronize()
     if pg:
@@ -280,6 +293,7 @@ def run_gpu(args):
 
     planner = None if args.no_e2e else run_planner(stream, args, dev)
     packed = None if args.no_e2e else run_packed(stream, args, dev)
+    baselines = None if args.no_e2e else run_baselines(pool, stream, args, dev, flops)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -293,13 +307,14 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD, "heads": H, "head_dim": D, "tokens_per_frame": T, "queries": nq,
                        "keys": nk, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
                        "parallelism": "replicas" if world > 1 else "single GPU",
+                       "stage_streams": n_streams,
                        "l2": "inputs larger than L2 (~440 MB touched per call)"},
             "pct_bf16_peak": round(100 * value / peaks["bf16_tflops"], 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
             "kernel_ms": {"publish_gather": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "packed": packed, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "packed": packed, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -343,6 +358,65 @@ def run_planner(stream, args, dev):
     flops = 4.0 * 4680 * 21 * T * D * H
     return {"workload": "planner block, 1.3B 480p shape, 21 context frames (W_ctx)", "queries": 4680,
             "keys": 21 * T, "ms_per_call": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+
+
+def run_baselines(pool, stream, args, dev, flops):
+    """Attention cost of one chunk-step (one layer) under FlashForward's schedule and
+    the cache-update-only schedules of Self-Forcing and HiAR, every call a steady
+    1.3B 480p ff_render_attn.  One GPU, attention only: context for the pages'
+    end-to-end multi-GPU speed-ups, not a reproduction of them."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff, schedules
+    T, H, D = 1560, 12, 128
+    S = 4
+    bb = ff.Bank(n_layers=1, n_stages=2 * S, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                 total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, planner_history=0, device=dev.index)
+    z = torch.zeros((3 * T, H, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(z)
+    for b in range(3):
+        bb.anchor_publish(0, 30 * b, 3, z, z, stream)
+    # bank slot of a call: denoise stage k -> bank k, re-encode k -> bank S + k
+    nxt = [0] * (2 * S)
+
+    def call(kind, k):
+        bank_stage = k if kind == "denoise" else S + (k % S)
+        i = nxt[bank_stage]
+        q, kk, v = pool[k % S][i % 4]
+        rc = bb.render_attn_raw(0, bank_stage, i, q.data_ptr(), kk.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"ff_render_attn failed with status {rc}")
+        nxt[bank_stage] += 1
+
+    # ramp every bank to steady state (5 chunks of history)
+    for st in range(2 * S):
+        for _ in range(5):
+            call("denoise" if st < S else "reencode", st)
+    res = {}
+    chunks = 4
+    for name, fn in schedules.SCHEDULES.items():
+        sched = fn(S)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(chunks):
+            for kind, k in sched:
+                call(kind, k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = {"calls_per_chunk_step": len(sched),
+                     "cache_update_only_calls": schedules.cache_update_only_calls(sched),
+                     "ms_per_chunk_step_per_layer": round(e0.elapsed_time(e1) / chunks, 4)}
+    assert bb.error_poll() == 0
+    bb.close()
+    base = res["flashforward"]["ms_per_chunk_step_per_layer"]
+    for name in ("self_forcing", "hiar"):
+        res[name]["time_vs_flashforward"] = round(res[name]["ms_per_chunk_step_per_layer"] / base, 3)
+    res["note"] = ("attention calls only, one layer, one GPU, S=4 stages; the pages report 1.42-2.92x vs "
+                   "Self-Forcing and 1.16-1.69x vs HiAR end to end with up to 4 GPUs")
+    return res
 
 
 def run_packed(stream, args, dev):
@@ -547,6 +621,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass (profiling runs)")
+    ap.add_argument("--stage-streams", type=int, default=1,
+                    help="CUDA streams the 4 stages are issued on (1..4); per-kernel event times need 1")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // running max m_s (log2 units), sum l_s and unnormalised O_s,
 //   m = max m_s,  l = sum l_s 2^(m_s - m),  O = sum O_s 2^(m_s - m) / l.
 template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 8;  // elements per thread
   const int unit = blockIdx.x;  // head * n_qb + linear query block
   const int head = unit / p.n_qb;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   while (g + 1 < p.n_groups && p.groups[g + 1].qb0 <= lin) ++g;
   const AttnGroup& G = p.groups[g];
   const int qb = lin - G.qb0;
-  const int rloc = blockIdx.y * 32 + (threadIdx.x >> 3);  // 0..255
+  const int rloc = blockIdx.y * 16 + (threadIdx.x >> 3);  // 0..255
   const int part = threadIdx.x & 7;
   const int lrow = qb * 256 + rloc;
   if (lrow >= G.nq) return;
@@ -473,10 +473,12 @@ size_t attention_smem_bytes(int head_dim) {
 }
 
 cudaError_t attention_configure(int head_dim) {
+  cudaError_t e;
   if (head_dim == 128)
-    return cudaFuncSetAttribute(bank_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                AttnCfg<128>::SMEM);
-  return cudaFuncSetAttribute(bank_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64>::SMEM);
+    e = cudaFuncSetAttribute(bank_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<128>::SMEM);
+  else
+    e = cudaFuncSetAttribute(bank_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64>::SMEM);
+  return e;
 }
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -489,11 +491,11 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensor
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
-  dim3 grid(p.heads * p.n_qb, 8);
+  dim3 grid(p.heads * p.n_qb, 16);  // 16 rows x 8 parts per 128-thread block
   if (head_dim == 128)
-    attn_combine_kernel<128><<<grid, 256, 0, s>>>(p);
+    attn_combine_kernel<128><<<grid, 128, 0, s>>>(p);
   else
-    attn_combine_kernel<64><<<grid, 256, 0, s>>>(p);
+    attn_combine_kernel<64><<<grid, 128, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -120,10 +120,10 @@ __device__ __forceinline__ int rope_index(const G1Params& p, int pair, int t, in
   return p.x_base + x * p.px + pair;
 }
 
-constexpr int kPubThreads = 256;
+constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 2;
 
-__global__ void __launch_bounds__(kPubThreads) publish_gather_kernel(const __grid_constant__ G1Params p) {
+__global__ void __launch_bounds__(kPubThreads, 8) publish_gather_kernel(const __grid_constant__ G1Params p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
   const int kind = I.kind;
