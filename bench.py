@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
 # a kernel edited since then reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (249.6e6, "ff_attn.cu", "25b0ad46f4b628a4"),
-    "publish_gather_kernel": (382.1e6, "ff_publish.cu", "922aef267f376fa4"),
+    "bank_attn_kernel": (246.9e6, "ff_attn.cu", "9f6e213b30cd87c5"),
+    "publish_gather_kernel": (382.2e6, "ff_publish.cu", "6760c7af2fb24807"),
 }
 
 

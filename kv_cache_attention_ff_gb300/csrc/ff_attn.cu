@@ -317,9 +317,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row max as a tree of 3-input maxima (8 independent chains)
+        float mk[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < 8; ++k) mk[k] = max3f(s[k], s[8 + k], s[16 + k]);
+#pragma unroll
+        for (int c = 24; c < 120; c += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mk[k] = max3f(mk[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], s[120 + k]);
+        const float mx = max3f(max3f(mk[0], mk[1], mk[2]), max3f(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
         const float m_new = mx * sl2;
         const bool need = m_new > m_run + 8.0f;
         float alpha = 1.0f;
@@ -328,14 +336,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m_run = m_new;
         }
         uint32_t pk[64];
-        float sum = 0.f;
+        const float neg_m = -m_run;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2_approx(__fmaf_rn(s[c], sl2, -m_run));
-          const float p1 = ex2_approx(__fmaf_rn(s[c + 1], sl2, -m_run));
-          sum += p0 + p1;
+          float a0, a1;
+          fma2(a0, a1, s[c], s[c + 1], sl2, neg_m);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          const int k = (c >> 1) & 3;
+          add2(acc[2 * k], acc[2 * k + 1], p0, p1);
           pk[c >> 1] = pack_bf16x2(p0, p1);
         }
+        const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l_run = __fmaf_rn(l_run, alpha, sum);
         if (j > 0) {
           if (!(ok = mbar_wait(o_done + t, n_od & 1, abort_flag, err))) break;

@@ -80,6 +80,8 @@ struct ff_bank {
   std::vector<Scratch> scratch;  // per stage
   Scratch planner;               // planner blocks (when planner_history > 0)
   int planner_max_pieces = 0;
+  size_t part_rows = 0;          // capacity of each stage's split partials, in rows
+  size_t planner_part_rows = 0;
   double2* rope64 = nullptr;
   float2* rope32 = nullptr;
   int rope_y_base = 0, rope_x_base = 0, pt = 0, py = 0, px = 0;
@@ -220,10 +222,10 @@ int cuda_err(cudaError_t e, const char* what) {
 }
 
 // 2-D tensor map over a bf16 [rows, heads * head_dim] buffer, 64 x 128 boxes, 128-byte swizzle.
-int make_map(const ff_bank* b, CUtensorMap* map, const void* base, int rows) {
+int make_map(const ff_bank* b, CUtensorMap* map, const void* base, int rows, int box_rows = 128) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(b->d.heads) * b->d.head_dim, static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(b->d.heads) * b->d.head_dim * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = b->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -232,6 +234,35 @@ int make_map(const ff_bank* b, CUtensorMap* map, const void* base, int rows) {
     FF_LOG("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return FF_ERR_CUDA;
   }
+  return FF_OK;
+}
+
+// Launch attention (and the split combine) for the query groups in `ap`
+// (heads, out, err, scale and groups filled by the caller).  Partial rows
+// beyond `part_rows` disable splitting.  With `tc`, ev[2] is recorded between
+// attention and combine.
+int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const void* k, const void* v, int k_rows,
+           float* part_o, float* part_ml, size_t part_rows, bool allow_split, cudaStream_t s, TimedCall* tc) {
+  const ff_bank_desc& d = b->d;
+  ap.part_o = part_o;
+  ap.part_ml = part_ml;
+  int rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(b, &tq, q, q_rows)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tv, v, k_rows)) != FF_OK) return rc;
+  if ((rc = make_map(b, &tk, k, k_rows)) != FF_OK) return rc;
+  if (ap.n_groups == 1 && allow_split) {
+    ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
+    if (static_cast<size_t>(d.heads) * ap.n_qb * ap.n_split * kQBlock > part_rows) ap.n_split = 1;
+  } else {
+    ap.n_split = 1;
+  }
+  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
+  const int grid = std::min(ap.n_pieces, b->sm_count);
+  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "attention launch")) != FF_OK) return rc;
+  if (tc) cudaEventRecord(tc->ev[2], s);
+  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
+  if (tc) tc->combine = ap.n_split > 1;
   return FF_OK;
 }
 
@@ -357,10 +388,16 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
     }
     return m;
   };
-  const int max_pieces = pieces_cap(d.chunk_frames, b->max_key_frames);
-  b->max_pieces = max_pieces;
+  // partial rows of key-range splits (256-row pieces)
+  auto rows_cap = [&](int q_frames, int k_frames) {
+    return static_cast<size_t>(pieces_cap(q_frames, k_frames)) * kQBlock;
+  };
+  b->part_rows = rows_cap(d.chunk_frames, b->max_key_frames);
   const int planner_frames = (d.planner_history + 1) * d.planner_block;
-  b->planner_max_pieces = d.planner_history > 0 ? pieces_cap(d.planner_block, planner_frames) : 0;
+  b->planner_part_rows = d.planner_history > 0 ? rows_cap(d.planner_block, planner_frames) : 0;
+  const int max_pieces = static_cast<int>(b->part_rows / kQBlock);
+  b->max_pieces = max_pieces;
+  b->planner_max_pieces = static_cast<int>(b->planner_part_rows / kQBlock);
 
   const int pt = (d.head_dim - 4 * (d.head_dim / 6)) / 2;
   const int py = (d.head_dim / 6);
@@ -720,18 +757,8 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   ap.err = b->err;
   ap.heads = d.heads;
   attn_single_group(ap, nq, nk);
-  ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
-  if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->max_pieces) ap.n_split = 1;
-  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
-  ap.part_o = sc.part_o;
-  ap.part_ml = sc.part_ml;
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
-
-  CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_map(b, &tq, sc.q_rot, nq)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tk, sc.ctx_k, nk)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tv, sc.ctx_v, nk)) != FF_OK) return rc;
 
   // ---- ordering against other streams
   wait_stage_events(b, s, stage);
@@ -746,13 +773,11 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   }
   if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
   if (b->timing) cudaEventRecord(tc.ev[1], s);
-  const int grid = std::min(ap.n_pieces, b->sm_count);
-  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "attention launch")) != FF_OK) return rc;
-  if (b->timing) cudaEventRecord(tc.ev[2], s);
-  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
+  if ((rc = attend(b, ap, sc.q_rot, nq, sc.ctx_k, sc.ctx_v, nk, sc.part_o, sc.part_ml, b->part_rows, true, s,
+                   b->timing ? &tc : nullptr)) != FF_OK)
+    return rc;
   if (b->timing) {
     cudaEventRecord(tc.ev[3], s);
-    tc.combine = ap.n_split > 1;
     b->timed.push_back(tc);
   }
   cudaEventRecord(b->ev_stage[stage], s);
@@ -840,26 +865,16 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
   ap.err = b->err;
   ap.heads = d.heads;
   attn_single_group(ap, nq, nk);
-  ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
-  if (static_cast<long long>(d.heads) * ap.n_qb * ap.n_split > b->planner_max_pieces) ap.n_split = 1;
-  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
-  ap.part_o = sc.part_o;
-  ap.part_ml = sc.part_ml;
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
-  CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_map(b, &tq, sc.q_rot, nq)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tk, sc.ctx_k, nk)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tv, sc.ctx_v, nk)) != FF_OK) return rc;
 
   if (b->planner_used && b->planner_stream != s) cudaStreamWaitEvent(s, b->ev_planner, 0);
   for (int j = 0; j < n_hist; ++j)
     if (b->anchor_used[hslots[j]] && b->anchor_stream[hslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[hslots[j]], 0);
   if ((rc = cuda_err(launch_publish(prm, 0, s), "planner gather launch")) != FF_OK) return rc;
-  const int grid = std::min(ap.n_pieces, b->sm_count);
-  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "planner attention launch")) != FF_OK)
+  if ((rc = attend(b, ap, sc.q_rot, nq, sc.ctx_k, sc.ctx_v, nk, sc.part_o, sc.part_ml, b->planner_part_rows, true, s,
+                   nullptr)) != FF_OK)
     return rc;
-  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "planner combine launch")) != FF_OK) return rc;
   cudaEventRecord(b->ev_planner, s);
   b->planner_stream = s;
   b->planner_used = true;
@@ -941,10 +956,6 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
   }
 
   // 2. block-causal attention: one query group per chunk, up to three key segments
-  CUtensorMap tq, tk, tv;
-  if ((rc = make_map(b, &tq, qrot, static_cast<int>(N * T))) != FF_OK) return rc;
-  if ((rc = make_map(b, &tk, kall, static_cast<int>((A + N) * T))) != FF_OK) return rc;
-  if ((rc = make_map(b, &tv, vall, static_cast<int>((A + N) * T))) != FF_OK) return rc;
   const int nc = n_chunks(d);
   for (int c0 = 0; c0 < nc; c0 += kMaxGroups) {
     const int c1 = std::min(nc, c0 + kMaxGroups);
@@ -979,9 +990,8 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       g.n_kv = tiles;
     }
     ap.n_qb = qb;
-    ap.n_pieces = d.heads * ap.n_qb;
-    const int grid = std::min(ap.n_pieces, b->sm_count);
-    if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "packed attention launch")) != FF_OK)
+    if ((rc = attend(b, ap, qrot, static_cast<int>(N * T), kall, vall, static_cast<int>((A + N) * T), nullptr, nullptr,
+                     0, false, s, nullptr)) != FF_OK)
       return rc;
   }
   return FF_OK;
@@ -995,7 +1005,7 @@ int ff_render_kernel_count(const ff_bank_t* b, int chunk, int* count) {
   const int n_qb = static_cast<int>((pl.n_frames * T + kQBlock - 1) / kQBlock);
   const int n_kv = static_cast<int>((pl.key_frames * T + kKTile - 1) / kKTile);
   int s = choose_split(b->d.heads * n_qb, n_kv, b->sm_count);
-  if (static_cast<long long>(b->d.heads) * n_qb * s > b->max_pieces) s = 1;
+  if (static_cast<size_t>(b->d.heads) * n_qb * s * kQBlock > b->part_rows) s = 1;
   *count = s > 1 ? 3 : 2;
   return FF_OK;
 }

@@ -115,4 +115,5 @@ size_t attention_smem_bytes(int head_dim);
 cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t attention_configure(int head_dim);
 
+
 }  // namespace ff
