@@ -1,13 +1,13 @@
 """Benchmark of the renderer bank-attention hot path on one GB300.
 
 A step is one ff_render_attn call of the Wan2.1-1.3B 480p workload at steady
-state: RoPE of the chunk's Q/K, publish of (K, V) into the stage bank, gather
-of 2 anchor + 15 history + 3 own latent frames (31200 keys), and attention of
-4680 queries x 12 heads x d 128 over them.  Steps rotate over the 4 stage banks
-(and over layers when more steps are asked for), always at chunks with full
-history.  Inputs are seeded synthetic tensors (AR(1) unit-RMS Q/K, N(0,1) V)
-already resident in HBM; each call touches ~440 MB, more than L2, so no extra
-flush is needed.
+state: RoPE of the chunk's Q/K, publish of (K, V) into the stage bank, and
+attention of 4680 queries x 12 heads x d 128 over 2 anchor + 15 history + 3 own
+latent frames (31200 keys), which the attention kernel gathers by reading the
+bank slots in place.  Steps rotate over the 4 stage banks (and over layers when
+more steps are asked for), always at chunks with full history.  Inputs are
+seeded synthetic tensors (AR(1) unit-RMS Q/K, N(0,1) V) already resident in
+HBM; each call touches ~300 MB, more than L2, so no extra flush is needed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
 
@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
 # a kernel edited since then reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (246.9e6, "ff_attn.cu", "9f6e213b30cd87c5"),
-    "publish_gather_kernel": (382.2e6, "ff_publish.cu", "6760c7af2fb24807"),
+    "bank_attn_kernel": (249.5e6, "ff_attn.cu", "f108e08e67bf3c3b"),
+    "rope_publish_kernel": (45.6e6, "ff_publish.cu", "431d5457a31f9d85"),
 }
 
 
@@ -79,9 +79,9 @@ def workload_numbers(T=1560, heads=12, d=128, nq_frames=3, key_frames=20):
     nq, nk = nq_frames * T, key_frames * T
     flops = 4.0 * nq * nk * d * heads
     F = T * heads * d * 2
-    # publish/gather algorithmic bytes per steady call: read q,k,v (9F) + anchors (4F)
-    # + history K/V (30F); write Q_rot (3F) + slot K/V (6F) + context K/V (40F)
-    g1_bytes = 92.0 * F
+    # RoPE/publish algorithmic bytes per steady call: read q, k, v (9F); write
+    # Q_rot (3F) and the slot's K, V (6F).  The context is not copied.
+    g1_bytes = 18.0 * F
     return nq, nk, flops, g1_bytes
 
 
@@ -282,10 +282,10 @@ def run_gpu(args):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(attn_tflops / peaks["bf16_tflops"], 4),
                 "traffic": ncu_traffic("bank_attn_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "algorithmic_per_launch": f"{flops / 1e9:.1f} GFLOP (4*Nq*Nk*d*h)", "avg_launch_ms": round(attn_ms, 4)}
-    roofline_publish = {"kernel": "publish_gather_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
+    roofline_publish = {"kernel": "rope_publish_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
-                        "traffic": ncu_traffic("publish_gather_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} hbm_gbs",
-                        "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (92 frames x 4.79 MB)",
+                        "traffic": ncu_traffic("rope_publish_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} hbm_gbs",
+                        "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (18 frames x 4.79 MB)",
                         "avg_launch_ms": round(pub_ms, 4)}
 
     # end to end: pinned host inputs -> device, call, output -> pinned host, every step
@@ -308,10 +308,10 @@ def run_gpu(args):
                        "keys": nk, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "stage_streams": n_streams,
-                       "l2": "inputs larger than L2 (~440 MB touched per call)"},
+                       "l2": "inputs larger than L2 (~300 MB touched per call)"},
             "pct_bf16_peak": round(100 * value / peaks["bf16_tflops"], 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
-            "kernel_ms": {"publish_gather": round(pub_ms, 4), "attention": round(attn_ms, 4),
+            "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
             "e2e": e2e, "planner": planner, "packed": packed, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,

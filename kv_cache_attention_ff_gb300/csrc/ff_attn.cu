@@ -1,8 +1,11 @@
 // Renderer bank attention on tcgen05 tensor cores.
 //
-// O = softmax(Q K^T / sqrt(d)) V per head over the gathered context
+// O = softmax(Q K^T / sqrt(d)) V per head over the context
 // [Gamma(i) anchors; last H stage-matched chunks; own chunk] (FlashForward,
 // onedev.kr/papers/332, "어떻게 동작하나", Eq. (2); no mask inside the key set).
+// The context is gathered by the K/V loads themselves: its frames are read in
+// place as up to kMaxSegs key segments (anchor-slot runs, stage-ring runs),
+// each through its own tensor map.
 // bf16 operands, fp32 accumulation in tensor memory, fp32 online softmax.
 //
 // One CTA per SM, 10 warps:
@@ -79,14 +82,15 @@ __device__ __forceinline__ Piece decode_piece(const AttnParams& p, int piece) {
   return r;
 }
 
-// Walks the key tiles of a group in order: for each tile its first key row and
-// the number of valid keys (<= 128; the rest of the tile belongs to another
-// segment or lies past the buffer).  Segment fields are reloaded only when a
-// segment ends.
+// Walks the key tiles of a group in order: for each tile its map, first key
+// row and the number of valid keys (<= 128; the rest of the tile belongs to
+// another segment or lies past the map).  Segment fields are reloaded only
+// when a segment ends.
 struct TileCursor {
-  int s, tw, row0, rows, end_tile;
+  int s, tw, map, row0, rows, end_tile;
 
   __device__ __forceinline__ void load(const AttnGroup& G) {
+    map = G.seg_map[s];
     row0 = G.seg_row0[s];
     rows = G.seg_rows[s];
     end_tile = (s + 1 < G.n_seg) ? G.seg_tile0[s + 1] : G.n_kv;
@@ -112,8 +116,8 @@ struct TileCursor {
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
+    bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ KVMaps kv,
+                     const __grid_constant__ AttnParams p) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,8 +165,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
+    for (int m = 0; m < kMaxMaps; ++m) {
+      tma_prefetch_desc(&kv.k[m]);
+      tma_prefetch_desc(&kv.v[m]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -201,9 +207,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t use = n_load / C::NST;
             if (use > 0 && !(ok = mbar_wait(kv_empty + stage, (use - 1) & 1, abort_flag, err))) break;
             mbar_expect_tx(kv_full + stage, C::KV_BYTES);
-            const CUtensorMap* map = is_k ? &tmK : &tmV;
+            TileCursor& cur = is_k ? kc : vc;
             int krow, kvalid;
-            (is_k ? kc : vc).next(G, kv0 + j, krow, kvalid);
+            cur.next(G, kv0 + j, krow, kvalid);
+            const CUtensorMap* map = is_k ? &kv.k[cur.map] : &kv.v[cur.map];
             for (int kb = 0; kb < C::KB; ++kb)
               tma_load_2d(sKV + stage * C::KV_BYTES + kb * C::BLK, map, head * D + kb * 64, krow, kv_full + stage);
             ++n_load;
@@ -494,12 +501,12 @@ cudaError_t attention_configure(int head_dim) {
   return e;
 }
 
-cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& kv, const AttnParams& p, int grid,
+                             cudaStream_t s) {
   if (head_dim == 128)
-    bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, tk, tv, p);
+    bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, p);
   else
-    bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, tk, tv, p);
+    bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
   return cudaGetLastError();
 }
 

@@ -1,12 +1,21 @@
 // Host side of libff: the bank state machine behind the C ABI in ff.h.
 //
 // State contract (FlashForward, onedev.kr/papers/332, "어떻게 동작하나", Eq. (2)):
-// stage bank B_k of each layer is a ring of H chunk slots; chunk i reads
-// B_k^(i) = chunks max(0, i-H) .. i-1 and leaves B_k^(i+1) = Tail_H(B_k^(i) U (i, K, V))
-// by writing slot i mod H.  Clean anchors (section "무엇과 다른가", stride Delta)
-// live in a per-layer ring of anchor slots, anchor a in slot (a / Delta) mod cap.
-// Gamma(i): nearest anchor at or before the chunk's first frame and nearest at
-// or after its last frame (dropped past the end; used once if both coincide).
+// stage bank B_k of each layer holds H chunks; chunk i reads
+// B_k^(i) = chunks max(0, i-H) .. i-1 and leaves B_k^(i+1) = Tail_H(B_k^(i) U (i, K, V)).
+// Clean anchors (section "무엇과 다른가", stride Delta) live in a per-layer ring
+// of anchor slots, anchor a in slot (a / Delta) mod cap.  Gamma(i): nearest
+// anchor at or before the chunk's first frame and nearest at or after its last
+// frame (dropped past the end; used once if both coincide).
+//
+// Storage: each (layer, stage) ring has H + 1 physical chunk slots, chunk j in
+// physical slot j mod (H + 1), so chunk i is written into the slot of chunk
+// i - H - 1, which no call reads any more, while chunks i - H .. i - 1 stay in
+// place for its attention.  Logical slot j mod H (the contract's slot) maps to
+// the physical slot of the resident chunk j.  K and V are separate planes
+// ([ring slots][B_R frames] each, likewise [cap][1 frame] for anchors), so
+// adjacent slots are adjacent rows and the attention reads the context as a
+// few row runs in place (no gather copy).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -47,6 +56,15 @@ struct SlotState {
   int frames = 0;
 };
 
+// A run of adjacent slots read as one key segment: plane 0 = anchor slots of
+// the layer, 1 = the (layer, stage) chunk ring, 2 = the planner's own-block
+// scratch; `frames` counts frames from the first slot's start.
+struct SegSpec {
+  int plane;
+  int slot;
+  int frames;
+};
+
 struct TimedCall {
   cudaEvent_t ev[4];
   bool combine;
@@ -67,13 +85,15 @@ struct ff_bank {
   size_t total_bytes = 0;
   std::vector<void*> allocations;
 
+  int ring = 0;              // physical chunk slots per (layer, stage): H + 1
+
   // device memory
-  uint8_t* stage_kv = nullptr;   // [L][S][H][2][B_R frames]
-  uint8_t* anchor_kv = nullptr;  // [L][cap][2][1 frame]
+  uint8_t* stage_kv = nullptr;   // [L][S][K, V][H + 1 slots][B_R frames]
+  uint8_t* anchor_kv = nullptr;  // [L][K, V][cap][1 frame]
   struct Scratch {
-    uint8_t* ctx_k = nullptr;
-    uint8_t* ctx_v = nullptr;
     uint8_t* q_rot = nullptr;
+    uint8_t* own_k = nullptr;    // planner: the block's rotated K, V
+    uint8_t* own_v = nullptr;
     float* part_o = nullptr;
     float* part_ml = nullptr;
   };
@@ -88,7 +108,7 @@ struct ff_bank {
   unsigned int* err = nullptr;
 
   // host state
-  std::vector<SlotState> stage_slots;   // [L][S][H]
+  std::vector<SlotState> stage_slots;   // [L][S][H + 1] physical slots
   std::vector<SlotState> anchor_slots;  // [L][cap]
   std::vector<int> next_chunk;          // [L][S]
 
@@ -109,25 +129,25 @@ struct ff_bank {
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 
-  SlotState& sslot(int l, int s, int h) { return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * d.history + h]; }
+  SlotState& sslot(int l, int s, int h) { return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * ring + h]; }
   const SlotState& sslot(int l, int s, int h) const {
-    return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * d.history + h];
+    return stage_slots[(static_cast<size_t>(l) * d.n_stages + s) * ring + h];
   }
   SlotState& aslot(int l, int a) { return anchor_slots[static_cast<size_t>(l) * d.anchor_capacity + a]; }
   const SlotState& aslot(int l, int a) const { return anchor_slots[static_cast<size_t>(l) * d.anchor_capacity + a]; }
 
   size_t slot_bytes() const { return static_cast<size_t>(d.chunk_frames) * frame_bytes; }
   uint8_t* stage_k(int l, int s, int h) const {
-    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * d.history + h) * 2 + 0) * slot_bytes();
+    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * 2 + 0) * ring + h) * slot_bytes();
   }
   uint8_t* stage_v(int l, int s, int h) const {
-    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * d.history + h) * 2 + 1) * slot_bytes();
+    return stage_kv + (((static_cast<size_t>(l) * d.n_stages + s) * 2 + 1) * ring + h) * slot_bytes();
   }
   uint8_t* anchor_k(int l, int a) const {
-    return anchor_kv + ((static_cast<size_t>(l) * d.anchor_capacity + a) * 2 + 0) * frame_bytes;
+    return anchor_kv + ((static_cast<size_t>(l) * 2 + 0) * d.anchor_capacity + a) * frame_bytes;
   }
   uint8_t* anchor_v(int l, int a) const {
-    return anchor_kv + ((static_cast<size_t>(l) * d.anchor_capacity + a) * 2 + 1) * frame_bytes;
+    return anchor_kv + ((static_cast<size_t>(l) * 2 + 1) * d.anchor_capacity + a) * frame_bytes;
   }
 };
 
@@ -237,20 +257,98 @@ int make_map(const ff_bank* b, CUtensorMap* map, const void* base, int rows, int
   return FF_OK;
 }
 
+// Append anchor slot `sl` (one frame) to `seg`, extending the last run when
+// the slot is physically next to it.
+void add_anchor_slot(std::vector<SegSpec>& seg, int sl) {
+  if (!seg.empty() && seg.back().plane == 0 && seg.back().slot + seg.back().frames == sl)
+    ++seg.back().frames;
+  else
+    seg.push_back({0, sl, 1});
+}
+
+// Key segments of chunk i: runs of adjacent anchor slots of Gamma(i), then runs
+// of adjacent ring slots holding chunks max(0, i-H) .. i (chunk j in physical
+// slot j mod (H+1)); a run continues past a slot only when that slot is full.
+std::vector<SegSpec> chunk_segments(const ff_bank_desc& d, int chunk, const ff_chunk_plan& pl) {
+  std::vector<SegSpec> seg;
+  for (int j = 0; j < pl.n_anchors; ++j) add_anchor_slot(seg, (pl.anchors[j] / d.anchor_stride) % d.anchor_capacity);
+  const int ring = d.history + 1;
+  std::vector<int> fr(ring, 0);
+  for (int j = pl.hist_first; j <= chunk; ++j) {
+    const int js = d.chunk_frames * j;
+    fr[j % ring] = std::min(js + d.chunk_frames - 1, d.total_frames - 1) - js + 1;
+  }
+  for (int h = 0; h < ring; ++h) {
+    if (!fr[h]) continue;
+    if (h > 0 && fr[h - 1] == d.chunk_frames && !seg.empty() && seg.back().plane == 1)
+      seg.back().frames += fr[h];
+    else
+      seg.push_back({1, h, fr[h]});
+  }
+  return seg;
+}
+
+// Key segments of planner block b: runs of the history blocks' anchor slots,
+// then the block's own rotated K/V (scratch).
+std::vector<SegSpec> planner_segments(const ff_bank_desc& d, const ff_planner_plan& pl) {
+  std::vector<SegSpec> seg;
+  for (int j = 0; j < pl.hist_frames; ++j)
+    add_anchor_slot(seg, (pl.hist_first_block * d.planner_block + j) % d.anchor_capacity);
+  seg.push_back({2, 0, pl.n_anchors});
+  return seg;
+}
+
+int tiles_of(const std::vector<SegSpec>& seg, long long T) {
+  int tiles = 0;
+  for (const SegSpec& g : seg) tiles += static_cast<int>((g.frames * T + kKTile - 1) / kKTile);
+  return tiles;
+}
+
+// Fill group `g`'s key segments and the launch's K/V maps (one pair per
+// segment, each ending where its segment ends).  `base` gives each segment's
+// first K and V frame.
+template <class Base>
+int build_segments(const ff_bank* b, const std::vector<SegSpec>& seg, Base base, AttnGroup& g, KVMaps& kv) {
+  if (seg.empty() || seg.size() > static_cast<size_t>(kMaxSegs)) return FF_ERR_ARG;
+  const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
+  g.n_seg = 0;
+  int tiles = 0;
+  for (const SegSpec& sp : seg) {
+    const void* k = nullptr;
+    const void* v = nullptr;
+    base(sp, &k, &v);
+    const long long rows = sp.frames * T;
+    const int m = g.n_seg;
+    int rc;
+    if ((rc = make_map(b, &kv.k[m], k, static_cast<int>(rows))) != FF_OK) return rc;
+    if ((rc = make_map(b, &kv.v[m], v, static_cast<int>(rows))) != FF_OK) return rc;
+    g.seg_map[m] = m;
+    g.seg_row0[m] = 0;
+    g.seg_rows[m] = static_cast<int>(rows);
+    g.seg_tile0[m] = tiles;
+    tiles += static_cast<int>((rows + kKTile - 1) / kKTile);
+    ++g.n_seg;
+  }
+  g.n_kv = tiles;
+  for (int m = g.n_seg; m < kMaxMaps; ++m) {  // unused entries stay valid descriptors
+    kv.k[m] = kv.k[0];
+    kv.v[m] = kv.v[0];
+  }
+  return FF_OK;
+}
+
 // Launch attention (and the split combine) for the query groups in `ap`
-// (heads, out, err, scale and groups filled by the caller).  Partial rows
-// beyond `part_rows` disable splitting.  With `tc`, ev[2] is recorded between
-// attention and combine.
-int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const void* k, const void* v, int k_rows,
-           float* part_o, float* part_ml, size_t part_rows, bool allow_split, cudaStream_t s, TimedCall* tc) {
+// (heads, out, err, scale and groups filled by the caller) over the K/V maps
+// `kv`.  Partial rows beyond `part_rows` disable splitting.  With `tc`, ev[2]
+// is recorded between attention and combine.
+int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const KVMaps& kv, float* part_o,
+           float* part_ml, size_t part_rows, bool allow_split, cudaStream_t s, TimedCall* tc) {
   const ff_bank_desc& d = b->d;
   ap.part_o = part_o;
   ap.part_ml = part_ml;
   int rc;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq;
   if ((rc = make_map(b, &tq, q, q_rows)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tv, v, k_rows)) != FF_OK) return rc;
-  if ((rc = make_map(b, &tk, k, k_rows)) != FF_OK) return rc;
   if (ap.n_groups == 1 && allow_split) {
     ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
     if (static_cast<size_t>(d.heads) * ap.n_qb * ap.n_split * kQBlock > part_rows) ap.n_split = 1;
@@ -259,11 +357,44 @@ int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const vo
   }
   ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
   const int grid = std::min(ap.n_pieces, b->sm_count);
-  if ((rc = cuda_err(launch_attention(d.head_dim, tq, tk, tv, ap, grid, s), "attention launch")) != FF_OK) return rc;
+  if ((rc = cuda_err(launch_attention(d.head_dim, tq, kv, ap, grid, s), "attention launch")) != FF_OK) return rc;
   if (tc) cudaEventRecord(tc->ev[2], s);
   if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
   if (tc) tc->combine = ap.n_split > 1;
   return FF_OK;
+}
+
+// Common fields of a RoPE/publish launch.
+G1Params publish_params(const ff_bank* b) {
+  const ff_bank_desc& d = b->d;
+  G1Params prm{};
+  prm.rope64 = b->rope64;
+  prm.rope32 = b->rope32;
+  prm.y_base = b->rope_y_base;
+  prm.x_base = b->rope_x_base;
+  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
+  prm.units_per_row = d.heads * d.head_dim / 8;
+  prm.units_per_head = d.head_dim / 8;
+  prm.frame_w = d.frame_w;
+  prm.pt = b->pt;
+  prm.py = b->py;
+  prm.px = b->px;
+  return prm;
+}
+
+G1Item rot_item(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int t, int q_frame) {
+  G1Item it{};
+  it.src_k = src_k;
+  it.src_v = src_v;
+  it.dst_k = dst_k;
+  it.dst_v = dst_v;
+  it.t = t;
+  it.q_frame = q_frame;
+  return it;
+}
+
+const uint8_t* frame_at(const void* base, size_t frame, size_t frame_bytes) {
+  return static_cast<const uint8_t*>(base) + frame * frame_bytes;
 }
 
 void free_all(ff_bank* b) {
@@ -373,18 +504,21 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   b->frame_elems = T * d.heads * d.head_dim;
   b->frame_bytes = b->frame_elems * 2;
   b->max_key_frames = 2 + (d.history + 1) * d.chunk_frames;
+  b->ring = d.history + 1;
 
-  // attention split scratch: the largest piece count any call of this bank can use
+  // attention split scratch: the largest piece count any call of this bank can
+  // use (a call's key tiles exceed ceil(keys / 128) by at most kMaxSegs - 1)
   auto pieces_cap = [&](int q_frames, int k_frames) {
     int m = 0;
     for (int f = 1; f <= q_frames; ++f) {
       const int nq = static_cast<int>(f * T);
       const int n_qb = (nq + kQBlock - 1) / kQBlock;
-      for (int kf = f; kf <= k_frames; ++kf) {
-        const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile);
-        const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
-        if (s > 1) m = std::max(m, d.heads * n_qb * s);
-      }
+      for (int kf = f; kf <= k_frames; ++kf)
+        for (int extra = 0; extra < kMaxSegs; ++extra) {
+          const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile) + extra;
+          const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
+          if (s > 1) m = std::max(m, d.heads * n_qb * s);
+        }
     }
     return m;
   };
@@ -409,20 +543,17 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   b->rope_x_base = b->rope_y_base + d.frame_h * py;
   const size_t n_rope = static_cast<size_t>(b->rope_x_base) + static_cast<size_t>(d.frame_w) * px;
 
-  const size_t stage_bytes = static_cast<size_t>(d.n_layers) * d.n_stages * d.history * 2 * b->slot_bytes();
+  const size_t stage_bytes = static_cast<size_t>(d.n_layers) * d.n_stages * b->ring * 2 * b->slot_bytes();
   const size_t anchor_bytes = static_cast<size_t>(d.n_layers) * d.anchor_capacity * 2 * b->frame_bytes;
-  const size_t ctx_bytes = static_cast<size_t>(b->max_key_frames) * b->frame_bytes;
   const size_t qrot_bytes = b->slot_bytes();
   const size_t part_o_bytes = static_cast<size_t>(max_pieces) * kQBlock * d.head_dim * 4;
   const size_t part_ml_bytes = static_cast<size_t>(max_pieces) * kQBlock * 8;
-  const size_t per_stage = 2 * ctx_bytes + qrot_bytes + part_o_bytes + part_ml_bytes;
+  const size_t per_stage = qrot_bytes + part_o_bytes + part_ml_bytes;
   const size_t rope_bytes = n_rope * (sizeof(double2) + sizeof(float2));
-  const size_t pl_ctx_bytes = static_cast<size_t>(planner_frames) * b->frame_bytes;
-  const size_t pl_qrot_bytes = static_cast<size_t>(d.planner_block) * b->frame_bytes;
+  const size_t pl_block_bytes = static_cast<size_t>(d.planner_block) * b->frame_bytes;
   const size_t pl_part_o_bytes = static_cast<size_t>(b->planner_max_pieces) * kQBlock * d.head_dim * 4;
   const size_t pl_part_ml_bytes = static_cast<size_t>(b->planner_max_pieces) * kQBlock * 8;
-  const size_t planner_bytes =
-      d.planner_history > 0 ? 2 * pl_ctx_bytes + pl_qrot_bytes + pl_part_o_bytes + pl_part_ml_bytes : 0;
+  const size_t planner_bytes = d.planner_history > 0 ? 3 * pl_block_bytes + pl_part_o_bytes + pl_part_ml_bytes : 0;
   b->total_bytes = stage_bytes + anchor_bytes + d.n_stages * per_stage + planner_bytes + rope_bytes + 256;
   if (d.max_bytes && b->total_bytes > d.max_bytes) {
     FF_LOG("bank needs %zu bytes > max_bytes %zu", b->total_bytes, d.max_bytes);
@@ -438,10 +569,6 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   b->anchor_kv = static_cast<uint8_t*>(p);
   b->scratch.resize(d.n_stages);
   for (int k = 0; k < d.n_stages; ++k) {
-    if ((rc = alloc(b, ctx_bytes, &p)) != FF_OK) goto fail;
-    b->scratch[k].ctx_k = static_cast<uint8_t*>(p);
-    if ((rc = alloc(b, ctx_bytes, &p)) != FF_OK) goto fail;
-    b->scratch[k].ctx_v = static_cast<uint8_t*>(p);
     if ((rc = alloc(b, qrot_bytes, &p)) != FF_OK) goto fail;
     b->scratch[k].q_rot = static_cast<uint8_t*>(p);
     if ((rc = alloc(b, part_o_bytes, &p)) != FF_OK) goto fail;
@@ -450,11 +577,11 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
     b->scratch[k].part_ml = static_cast<float*>(p);
   }
   if (d.planner_history > 0) {
-    if ((rc = alloc(b, pl_ctx_bytes, &p)) != FF_OK) goto fail;
-    b->planner.ctx_k = static_cast<uint8_t*>(p);
-    if ((rc = alloc(b, pl_ctx_bytes, &p)) != FF_OK) goto fail;
-    b->planner.ctx_v = static_cast<uint8_t*>(p);
-    if ((rc = alloc(b, pl_qrot_bytes, &p)) != FF_OK) goto fail;
+    if ((rc = alloc(b, pl_block_bytes, &p)) != FF_OK) goto fail;
+    b->planner.own_k = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, pl_block_bytes, &p)) != FF_OK) goto fail;
+    b->planner.own_v = static_cast<uint8_t*>(p);
+    if ((rc = alloc(b, pl_block_bytes, &p)) != FF_OK) goto fail;
     b->planner.q_rot = static_cast<uint8_t*>(p);
     if ((rc = alloc(b, pl_part_o_bytes, &p)) != FF_OK) goto fail;
     b->planner.part_o = static_cast<float*>(p);
@@ -508,7 +635,7 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
     goto fail;
   }
 
-  b->stage_slots.assign(static_cast<size_t>(d.n_layers) * d.n_stages * d.history, SlotState{});
+  b->stage_slots.assign(static_cast<size_t>(d.n_layers) * d.n_stages * b->ring, SlotState{});
   b->anchor_slots.assign(static_cast<size_t>(d.n_layers) * d.anchor_capacity, SlotState{});
   b->next_chunk.assign(static_cast<size_t>(d.n_layers) * d.n_stages, 0);
   b->ev_stage.assign(d.n_stages, nullptr);
@@ -577,11 +704,20 @@ int ff_bank_slot_info(const ff_bank_t* b, int layer, int stage, int slot, int* c
     return FF_OK;
   }
   if (slot < 0 || slot >= b->d.history) return FF_ERR_ARG;
-  const SlotState& s = b->sslot(layer, stage, slot);
-  if (chunk_tag) *chunk_tag = s.tag;
-  if (frames) *frames = s.frames;
-  if (k) *k = b->stage_k(layer, stage, slot);
-  if (v) *v = b->stage_v(layer, stage, slot);
+  // logical slot `slot` holds the resident chunk j (of the last H) with j mod H == slot
+  const int next = b->next_chunk[static_cast<size_t>(layer) * b->d.n_stages + stage];
+  int phys = slot, tag = -1, fr = 0;
+  for (int j = std::max(0, next - b->d.history); j < next; ++j)
+    if (j % b->d.history == slot) {
+      phys = j % b->ring;
+      const SlotState& s = b->sslot(layer, stage, phys);
+      tag = s.tag;
+      fr = s.frames;
+    }
+  if (chunk_tag) *chunk_tag = tag;
+  if (frames) *frames = fr;
+  if (k) *k = b->stage_k(layer, stage, phys);
+  if (v) *v = b->stage_v(layer, stage, phys);
   return FF_OK;
 }
 
@@ -605,7 +741,7 @@ int ff_bank_error_poll(ff_bank_t* b) {
 }
 
 int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_pre, const void* v, void* stream) {
-  if (!b || layer < 0 || layer >= b->d.n_layers || n < 1 || n > b->d.anchor_capacity || first < 0 ||
+  if (!b || layer < 0 || layer >= b->d.n_layers || n < 1 || n > b->d.anchor_capacity || n > kMaxItems || first < 0 ||
       first % b->d.anchor_stride != 0 || first + (n - 1) * b->d.anchor_stride > b->d.total_frames - 1 || !k_pre ||
       !v || !aligned16(k_pre) || !aligned16(v))
     return FF_ERR_ARG;
@@ -613,33 +749,13 @@ int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_p
   if (cudaSetDevice(b->d.device) != cudaSuccess) return FF_ERR_CUDA;
   const ff_bank_desc& d = b->d;
 
-  G1Params prm{};
-  prm.q_in = nullptr;
-  prm.k_in = k_pre;
-  prm.v_in = v;
-  prm.rope64 = b->rope64;
-  prm.rope32 = b->rope32;
-  prm.y_base = b->rope_y_base;
-  prm.x_base = b->rope_x_base;
-  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
-  prm.units_per_row = d.heads * d.head_dim / 8;
-  prm.units_per_head = d.head_dim / 8;
-  prm.frame_w = d.frame_w;
-  prm.pt = b->pt;
-  prm.py = b->py;
-  prm.px = b->px;
+  G1Params prm = publish_params(b);
   prm.n_items = n;
   for (int j = 0; j < n; ++j) {
     const int a = first + j * d.anchor_stride;
     const int sl = (a / d.anchor_stride) % d.anchor_capacity;
-    G1Item& it = prm.items[j];
-    it.kind = kItemAnchor;
-    it.k = b->anchor_k(layer, sl);
-    it.v = b->anchor_v(layer, sl);
-    it.ctx = -1;
-    it.r = j;
-    it.t = a;
-    it.old_ctx = -1;
+    prm.items[j] = rot_item(frame_at(k_pre, j, b->frame_bytes), frame_at(v, j, b->frame_bytes), b->anchor_k(layer, sl),
+                            b->anchor_v(layer, sl), a, -1);
   }
   // The slots may still be read by renders or planner blocks on other streams.
   wait_stage_events(b, s, -1);
@@ -677,88 +793,42 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
   ff_bank::Scratch& sc = b->scratch[stage];
+  const int own_phys = chunk % b->ring;
+  for (int jc = pl.hist_first; jc < chunk; ++jc)
+    if (b->sslot(layer, stage, jc % b->ring).tag != jc) return FF_ERR_ARG;  // internal invariant (Tail_H) broken
 
-  // ---- work items: context = [anchors ; history oldest..newest ; own]
-  G1Params prm{};
+  // ---- RoPE + publish of the own chunk into its ring slot
+  G1Params prm = publish_params(b);
   prm.q_in = q_pre;
-  prm.k_in = k_pre;
-  prm.v_in = v;
   prm.q_rot = sc.q_rot;
-  prm.ctx_k = sc.ctx_k;
-  prm.ctx_v = sc.ctx_v;
-  prm.rope64 = b->rope64;
-  prm.rope32 = b->rope32;
-  prm.y_base = b->rope_y_base;
-  prm.x_base = b->rope_x_base;
-  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
-  prm.units_per_row = d.heads * d.head_dim / 8;
-  prm.units_per_head = d.head_dim / 8;
-  prm.frame_w = d.frame_w;
-  prm.pt = b->pt;
-  prm.py = b->py;
-  prm.px = b->px;
-  int n_items = 0;
-  int ctx = 0;
-  for (int j = 0; j < pl.n_anchors; ++j) {
-    G1Item& it = prm.items[n_items++];
-    it.kind = kItemCopy;
-    it.k = b->anchor_k(layer, aslots[j]);
-    it.v = b->anchor_v(layer, aslots[j]);
-    it.ctx = ctx++;
-    it.r = it.t = 0;
-    it.old_ctx = -1;
-  }
-  // history; frames of the slot this chunk overwrites are saved by the own items
-  int old_ctx_first = -1, old_frames = 0;
-  for (int jc = pl.hist_first; jc < chunk; ++jc) {
-    const int hs = jc % d.history;
-    const SlotState& st = b->sslot(layer, stage, hs);
-    if (st.tag != jc) return FF_ERR_ARG;  // internal invariant (Tail_H) broken
-    const bool overwritten = (hs == pl.slot);
-    if (overwritten) {
-      old_ctx_first = ctx;
-      old_frames = st.frames;
-    }
-    for (int r = 0; r < st.frames; ++r) {
-      if (overwritten && r < pl.n_frames) {
-        ++ctx;  // written by own item r
-        continue;
-      }
-      G1Item& it = prm.items[n_items++];
-      it.kind = kItemCopy;
-      it.k = b->stage_k(layer, stage, hs) + static_cast<size_t>(r) * b->frame_bytes;
-      it.v = b->stage_v(layer, stage, hs) + static_cast<size_t>(r) * b->frame_bytes;
-      it.ctx = ctx++;
-      it.r = it.t = 0;
-      it.old_ctx = -1;
-    }
-  }
-  const int own_ctx = ctx;
-  for (int r = 0; r < pl.n_frames; ++r) {
-    G1Item& it = prm.items[n_items++];
-    it.kind = kItemOwn;
-    it.k = b->stage_k(layer, stage, pl.slot) + static_cast<size_t>(r) * b->frame_bytes;
-    it.v = b->stage_v(layer, stage, pl.slot) + static_cast<size_t>(r) * b->frame_bytes;
-    it.ctx = own_ctx + r;
-    it.r = r;
-    it.t = pl.first_frame + r;
-    it.old_ctx = (old_ctx_first >= 0 && r < old_frames) ? old_ctx_first + r : -1;
-  }
-  ctx += pl.n_frames;
-  prm.n_items = n_items;
-  if (ctx != pl.key_frames) return FF_ERR_ARG;
+  prm.n_items = pl.n_frames;
+  for (int r = 0; r < pl.n_frames; ++r)
+    prm.items[r] = rot_item(frame_at(k_pre, r, b->frame_bytes), frame_at(v, r, b->frame_bytes),
+                            b->stage_k(layer, stage, own_phys) + static_cast<size_t>(r) * b->frame_bytes,
+                            b->stage_v(layer, stage, own_phys) + static_cast<size_t>(r) * b->frame_bytes,
+                            pl.first_frame + r, r);
 
+  // ---- key segments, read in place: [anchor runs ; ring runs]
   const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
   const int nq = static_cast<int>(pl.n_frames * T);
-  const int nk = static_cast<int>(pl.key_frames * T);
-
   AttnParams ap{};
   ap.out = out;
   ap.err = b->err;
   ap.heads = d.heads;
-  attn_single_group(ap, nq, nk);
+  attn_single_group(ap, nq, 0);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
-  int rc;
+  KVMaps kv;
+  const std::vector<SegSpec> seg = chunk_segments(d, chunk, pl);
+  int key_frames = 0;
+  for (const SegSpec& g : seg) key_frames += g.frames;
+  if (key_frames != pl.key_frames) return FF_ERR_ARG;
+  int rc = build_segments(b, seg,
+                          [&](const SegSpec& g, const void** k, const void** vv) {
+                            *k = g.plane == 0 ? b->anchor_k(layer, g.slot) : b->stage_k(layer, stage, g.slot);
+                            *vv = g.plane == 0 ? b->anchor_v(layer, g.slot) : b->stage_v(layer, stage, g.slot);
+                          },
+                          ap.groups[0], kv);
+  if (rc != FF_OK) return rc;
 
   // ---- ordering against other streams
   wait_stage_events(b, s, stage);
@@ -773,8 +843,8 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   }
   if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
   if (b->timing) cudaEventRecord(tc.ev[1], s);
-  if ((rc = attend(b, ap, sc.q_rot, nq, sc.ctx_k, sc.ctx_v, nk, sc.part_o, sc.part_ml, b->part_rows, true, s,
-                   b->timing ? &tc : nullptr)) != FF_OK)
+  if ((rc = attend(b, ap, sc.q_rot, nq, kv, sc.part_o, sc.part_ml, b->part_rows, true, s, b->timing ? &tc : nullptr)) !=
+      FF_OK)
     return rc;
   if (b->timing) {
     cudaEventRecord(tc.ev[3], s);
@@ -784,7 +854,7 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   b->stage_stream[stage] = s;
   b->stage_used[stage] = true;
 
-  SlotState& own = b->sslot(layer, stage, pl.slot);
+  SlotState& own = b->sslot(layer, stage, own_phys);
   own.tag = chunk;
   own.frames = pl.n_frames;
   ++next;
@@ -817,63 +887,38 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
   if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
   ff_bank::Scratch& sc = b->planner;
 
-  G1Params prm{};
+  // RoPE of the block's Q, K, V into scratch; nothing is published
+  G1Params prm = publish_params(b);
   prm.q_in = q_pre;
-  prm.k_in = k_pre;
-  prm.v_in = v;
   prm.q_rot = sc.q_rot;
-  prm.ctx_k = sc.ctx_k;
-  prm.ctx_v = sc.ctx_v;
-  prm.rope64 = b->rope64;
-  prm.rope32 = b->rope32;
-  prm.y_base = b->rope_y_base;
-  prm.x_base = b->rope_x_base;
-  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
-  prm.units_per_row = d.heads * d.head_dim / 8;
-  prm.units_per_head = d.head_dim / 8;
-  prm.frame_w = d.frame_w;
-  prm.pt = b->pt;
-  prm.py = b->py;
-  prm.px = b->px;
-  int n_items = 0;
-  for (int j = 0; j < n_hist; ++j) {
-    G1Item& it = prm.items[n_items++];
-    it.kind = kItemCopy;
-    it.k = b->anchor_k(layer, hslots[j]);
-    it.v = b->anchor_v(layer, hslots[j]);
-    it.ctx = j;
-    it.r = it.t = 0;
-    it.old_ctx = -1;
-  }
-  for (int r = 0; r < pl.n_anchors; ++r) {
-    G1Item& it = prm.items[n_items++];
-    it.kind = kItemOwnCtx;
-    it.k = nullptr;
-    it.v = nullptr;
-    it.ctx = n_hist + r;
-    it.r = r;
-    it.t = (pl.first_anchor + r) * d.anchor_stride;
-    it.old_ctx = -1;
-  }
-  prm.n_items = n_items;
+  prm.n_items = pl.n_anchors;
+  for (int r = 0; r < pl.n_anchors; ++r)
+    prm.items[r] = rot_item(frame_at(k_pre, r, b->frame_bytes), frame_at(v, r, b->frame_bytes),
+                            sc.own_k + static_cast<size_t>(r) * b->frame_bytes,
+                            sc.own_v + static_cast<size_t>(r) * b->frame_bytes, (pl.first_anchor + r) * d.anchor_stride, r);
 
   const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
   const int nq = static_cast<int>(pl.n_anchors * T);
-  const int nk = static_cast<int>(pl.key_frames * T);
   AttnParams ap{};
   ap.out = out;
   ap.err = b->err;
   ap.heads = d.heads;
-  attn_single_group(ap, nq, nk);
+  attn_single_group(ap, nq, 0);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
-  int rc;
+  KVMaps kv;
+  int rc = build_segments(b, planner_segments(d, pl),
+                          [&](const SegSpec& g, const void** k, const void** vv) {
+                            *k = g.plane == 0 ? static_cast<const void*>(b->anchor_k(layer, g.slot)) : sc.own_k;
+                            *vv = g.plane == 0 ? static_cast<const void*>(b->anchor_v(layer, g.slot)) : sc.own_v;
+                          },
+                          ap.groups[0], kv);
+  if (rc != FF_OK) return rc;
 
   if (b->planner_used && b->planner_stream != s) cudaStreamWaitEvent(s, b->ev_planner, 0);
   for (int j = 0; j < n_hist; ++j)
     if (b->anchor_used[hslots[j]] && b->anchor_stream[hslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[hslots[j]], 0);
-  if ((rc = cuda_err(launch_publish(prm, 0, s), "planner gather launch")) != FF_OK) return rc;
-  if ((rc = attend(b, ap, sc.q_rot, nq, sc.ctx_k, sc.ctx_v, nk, sc.part_o, sc.part_ml, b->planner_part_rows, true, s,
-                   nullptr)) != FF_OK)
+  if ((rc = cuda_err(launch_publish(prm, 0, s), "planner rope launch")) != FF_OK) return rc;
+  if ((rc = attend(b, ap, sc.q_rot, nq, kv, sc.part_o, sc.part_ml, b->planner_part_rows, true, s, nullptr)) != FF_OK)
     return rc;
   cudaEventRecord(b->ev_planner, s);
   b->planner_stream = s;
@@ -910,46 +955,22 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
   uint8_t* qrot = ws + 2 * static_cast<size_t>(A + N) * b->frame_bytes;  // [N frames]
 
   // 1. rotary encoding of every anchor and frame into the workspace (batches of kMaxItems frames)
-  G1Params prm{};
-  prm.rope64 = b->rope64;
-  prm.rope32 = b->rope32;
-  prm.y_base = b->rope_y_base;
-  prm.x_base = b->rope_x_base;
-  prm.units_per_frame = static_cast<long long>(b->frame_elems / 8);
-  prm.units_per_row = d.heads * d.head_dim / 8;
-  prm.units_per_head = d.head_dim / 8;
-  prm.frame_w = d.frame_w;
-  prm.pt = b->pt;
-  prm.py = b->py;
-  prm.px = b->px;
-  prm.ctx_k = kall;
-  prm.ctx_v = vall;
+  G1Params prm = publish_params(b);
+  prm.q_in = q_pre;
+  prm.q_rot = qrot;
   int rc;
   for (int f0 = 0; f0 < A + N; f0 += kMaxItems) {
     const int f1 = std::min(A + N, f0 + kMaxItems);
-    // frames (not anchors) of this batch start at input frame max(f0, A) - A
-    const int first_frame = std::max(f0, A) - A;
-    prm.q_in = static_cast<const uint8_t*>(q_pre) + static_cast<size_t>(first_frame) * b->frame_bytes;
-    prm.k_in = static_cast<const uint8_t*>(k_pre) + static_cast<size_t>(first_frame) * b->frame_bytes;
-    prm.v_in = static_cast<const uint8_t*>(v) + static_cast<size_t>(first_frame) * b->frame_bytes;
-    prm.q_rot = qrot + static_cast<size_t>(first_frame) * b->frame_bytes;
     int n_items = 0;
     for (int f = f0; f < f1; ++f) {
-      G1Item& it = prm.items[n_items++];
-      it.ctx = f;
-      it.old_ctx = -1;
-      if (f < A) {
-        it.kind = kItemRotCtx;
-        it.k = static_cast<const uint8_t*>(anchor_k_pre) + static_cast<size_t>(f) * b->frame_bytes;
-        it.v = static_cast<const uint8_t*>(anchor_v) + static_cast<size_t>(f) * b->frame_bytes;
-        it.r = 0;
-        it.t = f * d.anchor_stride;
-      } else {
-        it.kind = kItemOwnCtx;
-        it.k = it.v = nullptr;
-        it.r = (f - A) - first_frame;
-        it.t = f - A;
-      }
+      uint8_t* dk = kall + static_cast<size_t>(f) * b->frame_bytes;
+      uint8_t* dv = vall + static_cast<size_t>(f) * b->frame_bytes;
+      if (f < A)
+        prm.items[n_items++] = rot_item(frame_at(anchor_k_pre, f, b->frame_bytes), frame_at(anchor_v, f, b->frame_bytes),
+                                        dk, dv, f * d.anchor_stride, -1);
+      else
+        prm.items[n_items++] = rot_item(frame_at(k_pre, f - A, b->frame_bytes), frame_at(v, f - A, b->frame_bytes), dk,
+                                        dv, f - A, f - A);
     }
     prm.n_items = n_items;
     if ((rc = cuda_err(launch_publish(prm, 0, s), "packed rope launch")) != FF_OK) return rc;
@@ -978,6 +999,7 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       g.n_seg = 0;
       int tiles = 0;
       auto add = [&](long long row0, long long rows) {
+        g.seg_map[g.n_seg] = 0;
         g.seg_row0[g.n_seg] = static_cast<int>(row0);
         g.seg_rows[g.n_seg] = static_cast<int>(rows);
         g.seg_tile0[g.n_seg] = tiles;
@@ -990,8 +1012,15 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       g.n_kv = tiles;
     }
     ap.n_qb = qb;
-    if ((rc = attend(b, ap, qrot, static_cast<int>(N * T), kall, vall, static_cast<int>((A + N) * T), nullptr, nullptr,
-                     0, false, s, nullptr)) != FF_OK)
+    KVMaps kv;
+    if ((rc = make_map(b, &kv.k[0], kall, static_cast<int>((A + N) * T))) != FF_OK ||
+        (rc = make_map(b, &kv.v[0], vall, static_cast<int>((A + N) * T))) != FF_OK)
+      return rc;
+    for (int m = 1; m < kMaxMaps; ++m) {
+      kv.k[m] = kv.k[0];
+      kv.v[m] = kv.v[0];
+    }
+    if ((rc = attend(b, ap, qrot, static_cast<int>(N * T), kv, nullptr, nullptr, 0, false, s, nullptr)) != FF_OK)
       return rc;
   }
   return FF_OK;
@@ -1003,7 +1032,7 @@ int ff_render_kernel_count(const ff_bank_t* b, int chunk, int* count) {
   plan(b->d, chunk, &pl);
   const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
   const int n_qb = static_cast<int>((pl.n_frames * T + kQBlock - 1) / kQBlock);
-  const int n_kv = static_cast<int>((pl.key_frames * T + kKTile - 1) / kKTile);
+  const int n_kv = tiles_of(chunk_segments(b->d, chunk, pl), T);
   int s = choose_split(b->d.heads * n_qb, n_kv, b->sm_count);
   if (static_cast<size_t>(b->d.heads) * n_qb * s * kQBlock > b->part_rows) s = 1;
   *count = s > 1 ? 3 : 2;

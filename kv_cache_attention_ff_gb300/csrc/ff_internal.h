@@ -9,40 +9,29 @@
 namespace ff {
 
 // ------------------------------------------------------------------ G1 / G2
-// One launch of the RoPE + publish + gather kernel processes a list of
-// frame-sized work items.  Every item covers one latent frame of one
-// tensor pair (K and V), T * heads * head_dim bf16 each, split into 16-byte
-// units; a thread handles the same unit offset of whatever an item touches.
-
-enum ItemKind : int {
-  kItemCopy = 0,    // context frame <- (k, v) source frame (anchor or history slot)
-  kItemOwn = 1,     // own chunk frame r: RoPE(q) -> q_rot, RoPE(k) and v -> slot frame r and context
-  kItemAnchor = 2,  // anchor input frame r: RoPE(k) and v -> anchor slot
-  kItemOwnCtx = 3,  // like kItemOwn but nothing is published (planner blocks, packed frames)
-  kItemRotCtx = 4,  // context frame <- (RoPE(k), v) of the source frame in (k, v); no Q, nothing published
-};
+// One launch of the RoPE + publish kernel processes a list of frame-sized work
+// items.  Every item covers one latent frame of one (K, V) pair,
+// T * heads * head_dim bf16 each, split into 16-byte units; a thread handles
+// the same unit offset of whatever an item touches.  An item reads a K and a V
+// frame, rotates K under the published-K contract and writes both to their
+// destination frames (a stage-ring slot, an anchor slot or a scratch buffer);
+// with q_frame >= 0 it also rotates frame q_frame of the Q input into the same
+// frame of q_rot.
 
 struct G1Item {
-  const void* k;   // copy: source K frame; own/anchor: destination K frame (slot)
-  const void* v;   // same for V
-  int kind;
-  int ctx;         // copy/own: context frame written (-1: none)
-  int r;           // own/anchor: frame index in the call's inputs
-  int t;           // own/anchor: absolute latent frame (rotary time position)
-  int old_ctx;     // own: context frame that receives the slot's previous content
-                   // before it is overwritten (-1: nothing to save)
-  int pad;
+  const void* src_k;  // K frame before rotary encoding
+  const void* src_v;  // V frame
+  void* dst_k;        // rotated K frame
+  void* dst_v;        // V frame (copied)
+  int t;              // absolute latent frame (rotary time position)
+  int q_frame;        // frame of q_in / q_rot to rotate, -1: none
 };
 
 constexpr int kMaxItems = 160;
 
 struct G1Params {
-  const void* q_in;   // own chunk inputs [F * T, h, d] (q unused for anchors)
-  const void* k_in;
-  const void* v_in;
+  const void* q_in;   // [F * T, h, d] queries before rotary encoding (or null)
   void* q_rot;        // [F * T, h, d]
-  void* ctx_k;        // [key_frames * T, h, d]
-  void* ctx_v;
   const double2* rope64;  // rotary (cos, sin) in fp64: [total_frames][pt], then [frame_h][py], then [frame_w][px]
   const float2* rope32;   // the same table rounded to fp32
   int y_base, x_base;     // first row-axis and column-axis entries
@@ -59,22 +48,33 @@ struct G1Params {
 // ----------------------------------------------------------------- attention
 
 // Attention work is described as query groups, each a run of query rows with
-// its own list of key segments (row ranges of the K/V buffers).  A renderer or
-// planner call is one group with one segment (the gathered context); a packed
-// block-causal forward has one group per chunk with up to three segments
-// (left anchor, right anchor, history + own chunk).
+// its own list of key segments.  A segment is a row range of one of the K/V
+// tensor-map pairs the launch carries.  A renderer call is one group whose
+// segments are read in place: runs of adjacent anchor slots and runs of
+// adjacent stage-ring slots, each with its own map whose extent ends at the
+// segment (rows past it read as zeros).  A planner call adds its own block from
+// scratch; a packed block-causal forward has one group per chunk, all
+// segments in one workspace map.
 constexpr int kMaxGroups = 96;
-constexpr int kMaxSegs = 3;
+constexpr int kMaxSegs = 4;
+constexpr int kMaxMaps = 4;
 
 struct AttnGroup {
   int q_row0;              // first query row of the group
   int nq;                  // query rows
   int qb0;                 // first linear 256-row query block of the group
   int n_seg;               // key segments (1..kMaxSegs)
-  int seg_row0[kMaxSegs];  // first key row of each segment
+  int seg_map[kMaxSegs];   // K/V map pair of each segment
+  int seg_row0[kMaxSegs];  // first key row of each segment within its map
   int seg_rows[kMaxSegs];  // key rows of each segment
   int seg_tile0[kMaxSegs]; // first 128-key tile of each segment in the group's tile sequence
   int n_kv;                // tiles over all segments
+};
+
+// K and V tensor maps of a launch (bf16 [rows, heads * head_dim], 64 x 128 boxes).
+struct KVMaps {
+  CUtensorMap k[kMaxMaps];
+  CUtensorMap v[kMaxMaps];
 };
 
 struct AttnParams {
@@ -91,7 +91,7 @@ struct AttnParams {
   AttnGroup groups[kMaxGroups];
 };
 
-// Fill `p` with the single group [0, nq) x one key segment [0, nk).
+// Fill `p` with the single group [0, nq) x one key segment [0, nk) of map 0.
 inline void attn_single_group(AttnParams& p, int nq, int nk) {
   p.n_groups = 1;
   AttnGroup& g = p.groups[0];
@@ -99,6 +99,7 @@ inline void attn_single_group(AttnParams& p, int nq, int nk) {
   g.nq = nq;
   g.qb0 = 0;
   g.n_seg = 1;
+  g.seg_map[0] = 0;
   g.seg_row0[0] = 0;
   g.seg_rows[0] = nk;
   g.seg_tile0[0] = 0;
@@ -108,8 +109,8 @@ inline void attn_single_group(AttnParams& p, int nq, int nk) {
 
 // Host launchers (ff_publish.cu / ff_attn.cu).
 cudaError_t launch_publish(const G1Params& p, int grid, cudaStream_t s);
-cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int grid, cudaStream_t s);
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& kv, const AttnParams& p, int grid,
+                             cudaStream_t s);
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s);
 size_t attention_smem_bytes(int head_dim);
 cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t s);

@@ -137,14 +137,19 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
   ap.part_ml = reinterpret_cast<float*>(base + kErrBytes + part_rows * head_dim * 4);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / __builtin_sqrt(static_cast<double>(head_dim)));
 
-  CUtensorMap tq, tk, tv;
-  if (map2d(&tq, q, nq, heads, head_dim) != FF_OK || map2d(&tk, k, nk, heads, head_dim) != FF_OK ||
-      map2d(&tv, v, nk, heads, head_dim) != FF_OK)
+  CUtensorMap tq;
+  ff::KVMaps kv;
+  if (map2d(&tq, q, nq, heads, head_dim) != FF_OK || map2d(&kv.k[0], k, nk, heads, head_dim) != FF_OK ||
+      map2d(&kv.v[0], v, nk, heads, head_dim) != FF_OK)
     return FF_ERR_CUDA;
+  for (int m = 1; m < ff::kMaxMaps; ++m) {
+    kv.k[m] = kv.k[0];
+    kv.v[m] = kv.v[0];
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ap.err, 0, sizeof(unsigned int), s) != cudaSuccess) return FF_ERR_CUDA;
   const int grid = ap.n_pieces < sms ? ap.n_pieces : sms;
-  if (ff::launch_attention(head_dim, tq, tk, tv, ap, grid, s) != cudaSuccess) return FF_ERR_CUDA;
+  if (ff::launch_attention(head_dim, tq, kv, ap, grid, s) != cudaSuccess) return FF_ERR_CUDA;
   if (ap.n_split > 1 && ff::launch_combine(head_dim, ap, s) != cudaSuccess) return FF_ERR_CUDA;
   return FF_OK;
 }

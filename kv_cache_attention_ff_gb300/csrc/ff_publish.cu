@@ -1,4 +1,4 @@
-// RoPE + publish + gather kernel (and its anchor-publish form).
+// RoPE + publish kernel (and its anchor-publish form).
 //
 // FlashForward renderer forward (onedev.kr/papers/332, "어떻게 동작하나", Eq. (2)):
 // the chunk's own K/V are computed by the denoising forward and published into
@@ -7,16 +7,11 @@
 // does the memory side of one such call:
 //   * RoPE of the chunk's Q (fp32 arithmetic, bf16 out) into a scratch buffer;
 //   * RoPE of the chunk's K under the published-K contract (below) and the
-//     store of (K, V) into bank slot i mod H;
-//   * the gather of [anchors; history; own] K/V into one contiguous context.
-// The same kernel serves anchor publishes (rotate at the anchor frame and store
-// into the anchor ring) and planner blocks (rotate the block and gather it after
-// the clean KV of the previous blocks, publishing nothing: the planner's clean
-// KV is published later by the block's cache-extraction forward).
-// The slot being overwritten still holds chunk i-H, which chunk i attends to:
-// the thread that writes unit u of the new chunk first reads unit u of the old
-// one and saves it into the context, so the read precedes the write in one
-// thread's program order (plain coherent loads for that slot).
+//     store of (K, V) into the chunk's stage-ring slot.
+// The gather of [anchors; history; own] is not a copy: the attention kernel
+// reads those frames where they live.  The same kernel serves anchor publishes
+// (rotate at the anchor frame and store into the anchor ring), planner blocks
+// and packed forwards (rotate into scratch, publishing nothing).
 //
 // Published-K contract: each rotated pair is
 //   a' = RNE_bf16(fl64(fl64(a c) - fl64(b s))),  b' = RNE_bf16(fl64(fl64(a s) + fl64(b c)))
@@ -101,11 +96,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
                : "l"(p));
   return r;
 }
-__device__ __forceinline__ uint4 ld_coherent(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
-  return r;
-}
 __device__ __forceinline__ void st_u4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
@@ -123,49 +113,19 @@ __device__ __forceinline__ int rope_index(const G1Params& p, int pair, int t, in
 constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 2;
 
-__global__ void __launch_bounds__(kPubThreads, 8) publish_gather_kernel(const __grid_constant__ G1Params p) {
+__global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __grid_constant__ G1Params p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
-  const int kind = I.kind;
-  const uint4* k_in = static_cast<const uint4*>(p.k_in);
-  const uint4* v_in = static_cast<const uint4*>(p.v_in);
-  const uint4* q_in = static_cast<const uint4*>(p.q_in);
-  uint4* ctx_k = static_cast<uint4*>(p.ctx_k);
-  uint4* ctx_v = static_cast<uint4*>(p.ctx_v);
-  uint4* slot_k = static_cast<uint4*>(const_cast<void*>(I.k));
-  uint4* slot_v = static_cast<uint4*>(const_cast<void*>(I.v));
+  const uint4* src_k = static_cast<const uint4*>(I.src_k);
+  const uint4* src_v = static_cast<const uint4*>(I.src_v);
+  uint4* dst_k = static_cast<uint4*>(I.dst_k);
+  uint4* dst_v = static_cast<uint4*>(I.dst_v);
+  const bool with_q = I.q_frame >= 0;
+  const size_t q_base = with_q ? static_cast<size_t>(I.q_frame) * upf : 0;
+  const uint4* q_in = static_cast<const uint4*>(p.q_in) + q_base;
+  uint4* q_out = static_cast<uint4*>(p.q_rot) + q_base;
 
   const int base = blockIdx.x * (kPubThreads * kPubUnroll) + threadIdx.x;
-  if (kind == kItemCopy) {
-    uint4 kk[kPubUnroll], vv[kPubUnroll];
-#pragma unroll
-    for (int j = 0; j < kPubUnroll; ++j) {
-      const int off = base + j * kPubThreads;
-      if (off < upf) {
-        kk[j] = ld_stream(slot_k + off);
-        vv[j] = ld_stream(slot_v + off);
-      }
-    }
-    const size_t cbase = static_cast<size_t>(I.ctx) * upf;
-#pragma unroll
-    for (int j = 0; j < kPubUnroll; ++j) {
-      const int off = base + j * kPubThreads;
-      if (off < upf) {
-        st_u4(ctx_k + cbase + off, kk[j]);
-        st_u4(ctx_v + cbase + off, vv[j]);
-      }
-    }
-    return;
-  }
-
-  // Own-chunk frame, planner-block or packed frame, anchor frame, or a rotated copy.
-  const bool own = (kind == kItemOwn) || (kind == kItemOwnCtx);
-  const bool rot_copy = (kind == kItemRotCtx);
-  const bool to_slot = (kind == kItemOwn) || (kind == kItemAnchor);
-  const bool save_old = (kind == kItemOwn) && I.old_ctx >= 0;
-  const size_t in_base = static_cast<size_t>(I.r) * upf;
-  const uint4* src_k = rot_copy ? slot_k : k_in + in_base;
-  const uint4* src_v = rot_copy ? slot_v : v_in + in_base;
 #pragma unroll
   for (int j = 0; j < kPubUnroll; ++j) {
     const int off = base + j * kPubThreads;
@@ -173,12 +133,7 @@ __global__ void __launch_bounds__(kPubThreads, 8) publish_gather_kernel(const __
     const uint4 kin = ld_stream(src_k + off);
     const uint4 vin = ld_stream(src_v + off);
     uint4 qin = make_uint4(0, 0, 0, 0);
-    if (own) qin = ld_stream(q_in + in_base + off);
-    uint4 oldk = make_uint4(0, 0, 0, 0), oldv = make_uint4(0, 0, 0, 0);
-    if (save_old) {  // read the slot's previous chunk before this thread overwrites it
-      oldk = ld_coherent(slot_k + off);
-      oldv = ld_coherent(slot_v + off);
-    }
+    if (with_q) qin = ld_stream(q_in + off);
     const int tok = off / p.units_per_row;
     const int in_row = off - tok * p.units_per_row;
     const int pair0 = (in_row % p.units_per_head) * 4;
@@ -202,29 +157,16 @@ __global__ void __launch_bounds__(kPubThreads, 8) publish_gather_kernel(const __
       const float qb2 = __fmaf_rn(qa, cs.y, __fmul_rn(qb, cs.x));
       qo[e] = bf16_bits(qa2) | (bf16_bits(qb2) << 16);
     }
-    const uint4 kout = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-    if (save_old) {
-      const size_t ob = static_cast<size_t>(I.old_ctx) * upf + off;
-      st_u4(ctx_k + ob, oldk);
-      st_u4(ctx_v + ob, oldv);
-    }
-    if (to_slot) {
-      st_u4(slot_k + off, kout);
-      st_u4(slot_v + off, vin);
-    }
-    if (own || rot_copy) {
-      const size_t cb = static_cast<size_t>(I.ctx) * upf + off;
-      st_u4(ctx_k + cb, kout);
-      st_u4(ctx_v + cb, vin);
-    }
-    if (own) st_u4(static_cast<uint4*>(p.q_rot) + in_base + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
+    st_u4(dst_k + off, make_uint4(ko[0], ko[1], ko[2], ko[3]));
+    st_u4(dst_v + off, vin);
+    if (with_q) st_u4(q_out + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
   }
 }
 
 cudaError_t launch_publish(const G1Params& p, int /*grid_hint*/, cudaStream_t s) {
   const int upf = static_cast<int>(p.units_per_frame);
   dim3 grid((upf + kPubThreads * kPubUnroll - 1) / (kPubThreads * kPubUnroll), p.n_items);
-  publish_gather_kernel<<<grid, kPubThreads, 0, s>>>(p);
+  rope_publish_kernel<<<grid, kPubThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
