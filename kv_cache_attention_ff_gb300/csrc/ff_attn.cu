@@ -14,8 +14,8 @@
 //   warp  8    TMA producer: Q tiles and a ring of K/V tiles
 //   warp  9    TMEM allocator and single-thread MMA issuer
 // Tensor memory (512 columns): S0 | S1 | O0 | O1 (S: 128 fp32 columns, O: d).
-// Per key tile j the MMA thread issues S0 = Q0 K_j^T, S1 = Q1 K_j^T, then
-// O0 += P0 V_{j-1}, O1 += P1 V_{j-1}: the tensor pipe works on one tile's
+// Per key tile j the MMA thread issues S0 = Q0 K_j^T, O0 += P0 V_{j-1},
+// S1 = Q1 K_j^T, O1 += P1 V_{j-1}: the tensor pipe works on one query tile's
 // products while the other warpgroup turns its scores into probabilities.
 // P goes through shared memory (bf16, 128-byte swizzled, K-major); V is read
 // MN-major straight from its TMA tile.  The running max is only raised when
@@ -59,6 +59,11 @@ struct AttnCfg {
 };
 
 constexpr int kAttnThreads = 320;
+// K/V tiles are prefetched into L2 this many tiles ahead of their loads.  The
+// CTAs working on one (head, key range) stream the same tiles together, so a
+// tile's first touch would otherwise stall all of them on a DRAM round trip;
+// tile t is prefetched by the CTA whose query block is t mod (query blocks).
+constexpr int kPrefetchTiles = 6;
 
 // Piece -> (head, group, query block of the group, key-tile range).
 struct Piece {
@@ -193,11 +198,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_2d(sQ + t * C::Q_BYTES + kb * C::BLK, &tmQ, head * D + kb * 64,
                         G.q_row0 + pc.qb * 256 + t * 128, q_full);
         const int n = kv1 - kv0;
+        // L2 prefetch of tile u of the piece, if this CTA's query block owns it
+        const int n_qb_g = (G.nq + 255) / 256;
+        TileCursor pfc;
+        pfc.start(G, kv0);
+        auto prefetch = [&](int u) {
+          int prow, pvalid;
+          pfc.next(G, kv0 + u, prow, pvalid);
+          if ((kv0 + u) % n_qb_g != pc.qb) return;
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_prefetch_l2_2d(&kv.k[pfc.map], head * D + kb * 64, prow);
+            tma_prefetch_l2_2d(&kv.v[pfc.map], head * D + kb * 64, prow);
+          }
+        };
+        for (int u = 0; u < kPrefetchTiles && u < n; ++u) prefetch(u);
         // consumption order: K_0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}
         TileCursor kc, vc;
         kc.start(G, kv0);
         vc.start(G, kv0);
         for (int step = 0; step <= n && ok; ++step) {
+          if (step + kPrefetchTiles < n) prefetch(step + kPrefetchTiles);
           for (int which = 0; which < 2; ++which) {
             const bool is_k = (which == 0);
             const int j = is_k ? step : step - 1;
@@ -228,60 +248,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int seg = 0;
       bool ok = true;
 
-      auto pv = [&](int jj, int head_seg) -> bool {
-        const int stage = static_cast<int>(n_kvc % C::NST);
-        if (!mbar_wait(kv_full + stage, (n_kvc / C::NST) & 1, abort_flag, err)) return false;
+      // S_t = Q_t K^T for the K tile at `ka`, once softmax t has read the previous S_t
+      auto s_mma = [&](int t, uint32_t ka) -> bool {
+        if (n_s[t] > 0 && !mbar_wait(s_free + t, (n_s[t] - 1) & 1, abort_flag, err)) return false;
         tc_fence_after();
-        const uint32_t va = sKVa + stage * C::KV_BYTES;
-        for (int t = 0; t < 2; ++t) {
-          if (jj == 0 && head_seg > 0 && !mbar_wait(o_free + t, (head_seg - 1) & 1, abort_flag, err)) return false;
-          if (!mbar_wait(p_full + t, n_pv[t] & 1, abort_flag, err)) return false;
-          tc_fence_after();
-          const uint32_t pa = sPa + t * C::P_BYTES;
+        const uint32_t qa = sQa + t * C::Q_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc(pa + (kk >> 2) * C::BLK + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(va + kk * 2048, C::BLK, 1024);
-            mma_bf16_ss(tmem + C::TMEM_O + t * D, ad, bd, kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(o_done + t);
-          ++n_pv[t];
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TMEM_S + t * 128, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), kIdescS,
+                      kk > 0 ? 1u : 0u);
         }
-        mma_commit(kv_empty + stage);
-        ++n_kvc;
+        mma_commit(s_full + t);
+        ++n_s[t];
         return true;
       };
+      // O_t (+)= P_t V for the V tile at `va`, once P_t is stored (and, for the
+      // first tile of a piece, once the previous piece's O_t has been read out)
+      auto pv_mma = [&](int t, uint32_t va, bool first, int head_seg) -> bool {
+        if (first && head_seg > 0 && !mbar_wait(o_free + t, (head_seg - 1) & 1, abort_flag, err)) return false;
+        if (!mbar_wait(p_full + t, n_pv[t] & 1, abort_flag, err)) return false;
+        tc_fence_after();
+        const uint32_t pa = sPa + t * C::P_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc(pa + (kk >> 2) * C::BLK + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc(va + kk * 2048, C::BLK, 1024);
+          mma_bf16_ss(tmem + C::TMEM_O + t * D, ad, bd, kIdescO, (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done + t);
+        ++n_pv[t];
+        return true;
+      };
+      // K/V ring entry `li` (in load order): wait for its data, return its address
+      auto kv_ready = [&](uint32_t li, uint32_t& addr) -> bool {
+        const int stage = static_cast<int>(li % C::NST);
+        if (!mbar_wait(kv_full + stage, (li / C::NST) & 1, abort_flag, err)) return false;
+        tc_fence_after();
+        addr = sKVa + stage * C::KV_BYTES;
+        return true;
+      };
+      auto kv_release = [&](uint32_t li) { mma_commit(kv_empty + static_cast<int>(li % C::NST)); };
 
+      // Issue order per key tile j: S0(j), PV0(j-1), S1(j), PV1(j-1).  Each S
+      // is issued as soon as its softmax warpgroup has read the previous one,
+      // and the two query tiles' products alternate on the tensor pipe, so the
+      // two softmax warpgroups run half a tile apart.
       for (int piece = blockIdx.x; piece < p.n_pieces && ok; piece += gridDim.x, ++seg) {
         const Piece pc = decode_piece(p, piece);
         const int n = pc.kv1 - pc.kv0;
         if (!(ok = mbar_wait(q_full, seg & 1, abort_flag, err))) break;
         tc_fence_after();
+        uint32_t ka = 0, va = 0;
         for (int j = 0; j < n && ok; ++j) {
-          const int stage = static_cast<int>(n_kvc % C::NST);
-          if (!(ok = mbar_wait(kv_full + stage, (n_kvc / C::NST) & 1, abort_flag, err))) break;
-          tc_fence_after();
-          const uint32_t ka = sKVa + stage * C::KV_BYTES;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (n_s[t] > 0 && !(ok = mbar_wait(s_free + t, (n_s[t] - 1) & 1, abort_flag, err))) break;
-            tc_fence_after();
-            const uint32_t qa = sQa + t * C::Q_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
-              mma_bf16_ss(tmem + C::TMEM_S + t * 128, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024),
-                          kIdescS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(s_full + t);
-            ++n_s[t];
-          }
-          if (!ok) break;
-          mma_commit(kv_empty + stage);
-          ++n_kvc;
+          const uint32_t ek = n_kvc;  // K_j; V_{j-1} follows it in the ring
+          if (!(ok = kv_ready(ek, ka) && s_mma(0, ka))) break;
+          if (j >= 1 && !(ok = kv_ready(ek + 1, va) && pv_mma(0, va, j == 1, seg))) break;
+          if (!(ok = s_mma(1, ka))) break;
+          kv_release(ek);
           if (j == n - 1) mma_commit(q_empty);
-          if (j >= 1) ok = pv(j - 1, seg);
+          if (j >= 1) {
+            if (!(ok = pv_mma(1, va, j == 1, seg))) break;
+            kv_release(ek + 1);
+          }
+          n_kvc += (j >= 1) ? 2 : 1;
         }
-        if (ok) ok = pv(n - 1, seg);
+        if (!ok) break;
+        // V_{n-1}
+        if (!(ok = kv_ready(n_kvc, va) && pv_mma(0, va, n == 1, seg) && pv_mma(1, va, n == 1, seg))) break;
+        kv_release(n_kvc);
+        ++n_kvc;
       }
       mma_commit(fin);
       mbar_wait(fin, 0, abort_flag, err);
