@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
 # a kernel edited since then reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (249.5e6, "ff_attn.cu", "f108e08e67bf3c3b"),
+    "bank_attn_kernel": (246.9e6, "ff_attn.cu", "37587878536567b2"),
     "rope_publish_kernel": (45.6e6, "ff_publish.cu", "431d5457a31f9d85"),
 }
 
