@@ -23,12 +23,12 @@
 // final normalisation uses the same stale max, which keeps the result exact
 // up to rounding.
 //
-// Work split: a (head, query block) unit covers n_kv key tiles; units are cut
-// into n_split key ranges ("pieces") so that pieces fill whole waves of SMs.
-// Pieces are ordered (head, split, query block) and taken round-robin by the
-// persistent CTAs, so concurrently running CTAs stream the same key tiles
-// (L2 reuse).  Split pieces write unnormalised partials that a small combine
-// kernel merges.
+// Work split: a (head, query block) unit covers n_kv key tiles.  The first
+// n_whole units run as one piece each; the rest are cut into n_split key
+// ranges, so that the persistent CTAs (taking pieces round-robin) finish
+// together.  Units are ordered (head, query block), split pieces (split, unit),
+// so concurrently running CTAs stream the same key tiles (L2 reuse).  Split
+// pieces write unnormalised partials that a small combine kernel merges.
 #include <cuda_bf16.h>
 
 #include "ff_internal.h"
@@ -65,25 +65,37 @@ constexpr int kAttnThreads = 320;
 // tile t is prefetched by the CTA whose query block is t mod (query blocks).
 constexpr int kPrefetchTiles = 6;
 
-// Piece -> (head, group, query block of the group, key-tile range).
+// Piece -> (head, group, query block of the group, key-tile range, partial
+// slot: -1 for a whole unit, else the split piece's index).
 struct Piece {
-  int head, g, qb, kv0, kv1;
+  int head, g, qb, kv0, kv1, part;
 };
 
 __device__ __forceinline__ Piece decode_piece(const AttnParams& p, int piece) {
   Piece r;
-  const int per_head = p.n_split * p.n_qb;
-  r.head = piece / per_head;
-  const int rem = piece - r.head * per_head;
-  const int split = rem / p.n_qb;
-  const int lin = rem - split * p.n_qb;
+  int unit, split, ns;
+  if (piece < p.n_whole) {
+    unit = piece;
+    split = 0;
+    ns = 1;
+    r.part = -1;
+  } else {
+    const int q = piece - p.n_whole;
+    const int rest = p.heads * p.n_qb - p.n_whole;
+    split = q / rest;
+    unit = p.n_whole + (q - split * rest);
+    ns = p.n_split;
+    r.part = q;
+  }
+  r.head = unit / p.n_qb;
+  const int lin = unit - r.head * p.n_qb;
   int g = 0;
   while (g + 1 < p.n_groups && p.groups[g + 1].qb0 <= lin) ++g;
   r.g = g;
   r.qb = lin - p.groups[g].qb0;
   const int nkv = p.groups[g].n_kv;
-  r.kv0 = static_cast<int>((static_cast<long long>(split) * nkv) / p.n_split);
-  r.kv1 = static_cast<int>((static_cast<long long>(split + 1) * nkv) / p.n_split);
+  r.kv0 = static_cast<int>((static_cast<long long>(split) * nkv) / ns);
+  r.kv1 = static_cast<int>((static_cast<long long>(split + 1) * nkv) / ns);
   return r;
 }
 
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ++n_od;
       tc_fence_after();
       const int lrow = pc.qb * 256 + t * 128 + r;  // row within the group
-      if (p.n_split == 1) {
+      if (pc.part < 0) {
         const float inv = 1.0f / l_run;
         __nv_bfloat16* dst =
             static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(G.q_row0 + lrow) * p.heads + head) * D;
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       } else {
-        const size_t prow = static_cast<size_t>(piece) * 256 + t * 128 + r;
+        const size_t prow = static_cast<size_t>(pc.part) * 256 + t * 128 + r;
         float* dst = p.part_o + prow * D;
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
@@ -477,7 +489,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 8;  // elements per thread
-  const int unit = blockIdx.x;  // head * n_qb + linear query block
+  const int rest = p.heads * p.n_qb - p.n_whole;  // split units
+  const int ru = blockIdx.x;                       // index among the split units
+  const int unit = p.n_whole + ru;                 // head * n_qb + linear query block
   const int head = unit / p.n_qb;
   const int lin = unit - head * p.n_qb;
   int g = 0;
@@ -492,7 +506,7 @@ __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_const
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   float m = -INFINITY;
   for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + lin;
+    const size_t piece = static_cast<size_t>(s) * rest + ru;
     m = fmaxf(m, ml[piece * 256 + rloc].x);
   }
   float acc[PER];
@@ -500,7 +514,7 @@ __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_const
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f;
   for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = (static_cast<size_t>(head) * p.n_split + s) * p.n_qb + lin;
+    const size_t piece = static_cast<size_t>(s) * rest + ru;
     const float2 v = ml[piece * 256 + rloc];
     const float w = exp2f(v.x - m);
     l = __fmaf_rn(v.y, w, l);
@@ -547,7 +561,7 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& 
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
-  dim3 grid(p.heads * p.n_qb, 16);  // 16 rows x 8 parts per 128-thread block
+  dim3 grid(p.heads * p.n_qb - p.n_whole, 16);  // split units; 16 rows x 8 parts per 128-thread block
   if (head_dim == 128)
     attn_combine_kernel<128><<<grid, 128, 0, s>>>(p);
   else

@@ -216,21 +216,50 @@ void plan_planner(const ff_bank_desc& d, int b, ff_planner_plan* p) {
   p->key_frames = p->hist_frames + p->n_anchors;
 }
 
-// Key-range splits per (head, query block) so that pieces fill the SMs:
-// minimise waves * (tiles per piece + per-piece overhead) + combine cost.
-int choose_split(int units, int n_kv, int sms) {
-  double best = 1e300;
-  int best_s = 1;
-  for (int s = 1; s <= std::min(4, n_kv); ++s) {
-    const long long pieces = static_cast<long long>(units) * s;
-    const long long waves = (pieces + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0) + (s > 1 ? 4.0 : 0.0);
-    if (cost < best - 1e-9) {
-      best = cost;
-      best_s = s;
+// Work plan of an attention call with `units` (head, query block) units of
+// n_kv key tiles on `sms` persistent CTAs: the first n_whole units run as one
+// piece each, the others as n_split key ranges merged by the combine kernel.
+// Candidates are whole waves of whole units followed by split units; each is
+// scored by the round-robin makespan in tiles (+2 per piece for its prologue
+// and epilogue) plus the combine's cost (about 1e-4 tile per partial row).
+struct SplitPlan {
+  int n_whole, n_split, n_pieces;
+  size_t part_rows;
+};
+
+SplitPlan plan_split(int units, int n_kv, int sms, size_t max_part_rows) {
+  SplitPlan best{units, 1, units, 0};
+  double best_cost = 1e300;
+  std::vector<double> load(static_cast<size_t>(std::max(sms, 1)));
+  for (int ns = 1; ns <= std::min(4, n_kv); ++ns) {
+    for (int m = 0; m * sms <= units; ++m) {
+      const int n_whole = (ns == 1) ? units : m * sms;
+      const int rest = units - n_whole;
+      if (ns > 1 && rest == 0) continue;
+      const size_t rows = static_cast<size_t>(rest) * ns * 256;
+      if (ns > 1 && rows > max_part_rows) continue;
+      const int pieces = n_whole + rest * ns;
+      const int grid = std::min(pieces, sms);
+      std::fill(load.begin(), load.begin() + grid, 0.0);
+      for (int pc = 0; pc < pieces; ++pc) {
+        int tiles = n_kv;
+        if (pc >= n_whole) {
+          const int split = (pc - n_whole) / rest;
+          tiles = static_cast<int>((static_cast<long long>(split + 1) * n_kv) / ns -
+                                   (static_cast<long long>(split) * n_kv) / ns);
+        }
+        load[pc % grid] += tiles + 2.0;
+      }
+      double cost = *std::max_element(load.begin(), load.begin() + grid);
+      if (ns > 1) cost += 4.0 + static_cast<double>(rows) * 1e-4;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = {n_whole, ns, pieces, ns > 1 ? rows : 0};
+      }
+      if (ns == 1) break;
     }
   }
-  return best_s;
+  return best;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -349,13 +378,12 @@ int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const KV
   int rc;
   CUtensorMap tq;
   if ((rc = make_map(b, &tq, q, q_rows)) != FF_OK) return rc;
-  if (ap.n_groups == 1 && allow_split) {
-    ap.n_split = choose_split(d.heads * ap.n_qb, ap.groups[0].n_kv, b->sm_count);
-    if (static_cast<size_t>(d.heads) * ap.n_qb * ap.n_split * kQBlock > part_rows) ap.n_split = 1;
-  } else {
-    ap.n_split = 1;
-  }
-  ap.n_pieces = d.heads * ap.n_qb * ap.n_split;
+  const int units = d.heads * ap.n_qb;
+  SplitPlan sp{units, 1, units, 0};
+  if (ap.n_groups == 1 && allow_split) sp = plan_split(units, ap.groups[0].n_kv, b->sm_count, part_rows);
+  ap.n_whole = sp.n_whole;
+  ap.n_split = sp.n_split;
+  ap.n_pieces = sp.n_pieces;
   const int grid = std::min(ap.n_pieces, b->sm_count);
   if ((rc = cuda_err(launch_attention(d.head_dim, tq, kv, ap, grid, s), "attention launch")) != FF_OK) return rc;
   if (tc) cudaEventRecord(tc->ev[2], s);
@@ -506,25 +534,20 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   b->max_key_frames = 2 + (d.history + 1) * d.chunk_frames;
   b->ring = d.history + 1;
 
-  // attention split scratch: the largest piece count any call of this bank can
+  // attention split scratch: the most partial rows any call of this bank can
   // use (a call's key tiles exceed ceil(keys / 128) by at most kMaxSegs - 1)
-  auto pieces_cap = [&](int q_frames, int k_frames) {
-    int m = 0;
+  auto rows_cap = [&](int q_frames, int k_frames) {
+    size_t m = 0;
     for (int f = 1; f <= q_frames; ++f) {
       const int nq = static_cast<int>(f * T);
       const int n_qb = (nq + kQBlock - 1) / kQBlock;
       for (int kf = f; kf <= k_frames; ++kf)
         for (int extra = 0; extra < kMaxSegs; ++extra) {
           const int n_kv = static_cast<int>((kf * T + kKTile - 1) / kKTile) + extra;
-          const int s = choose_split(d.heads * n_qb, n_kv, b->sm_count);
-          if (s > 1) m = std::max(m, d.heads * n_qb * s);
+          m = std::max(m, plan_split(d.heads * n_qb, n_kv, b->sm_count, static_cast<size_t>(-1)).part_rows);
         }
     }
     return m;
-  };
-  // partial rows of key-range splits (256-row pieces)
-  auto rows_cap = [&](int q_frames, int k_frames) {
-    return static_cast<size_t>(pieces_cap(q_frames, k_frames)) * kQBlock;
   };
   b->part_rows = rows_cap(d.chunk_frames, b->max_key_frames);
   const int planner_frames = (d.planner_history + 1) * d.planner_block;
@@ -1033,9 +1056,8 @@ int ff_render_kernel_count(const ff_bank_t* b, int chunk, int* count) {
   const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
   const int n_qb = static_cast<int>((pl.n_frames * T + kQBlock - 1) / kQBlock);
   const int n_kv = tiles_of(chunk_segments(b->d, chunk, pl), T);
-  int s = choose_split(b->d.heads * n_qb, n_kv, b->sm_count);
-  if (static_cast<size_t>(b->d.heads) * n_qb * s * kQBlock > b->part_rows) s = 1;
-  *count = s > 1 ? 3 : 2;
+  const SplitPlan sp = plan_split(b->d.heads * n_qb, n_kv, b->sm_count, b->part_rows);
+  *count = sp.n_split > 1 ? 3 : 2;
   return FF_OK;
 }
 

@@ -79,13 +79,19 @@ struct KVMaps {
 
 struct AttnParams {
   void* out;            // bf16 [query rows, h, d]
-  float* part_o;        // [pieces][256][d] unnormalised partial outputs (split only)
-  float* part_ml;       // [pieces][256][2] running max (log2 units) and sum
+  float* part_o;        // [split pieces][256][d] unnormalised partial outputs
+  float* part_ml;       // [split pieces][256][2] running max (log2 units) and sum
   unsigned int* err;    // device error word
   int heads;
   int n_qb;             // linear 256-row query blocks over all groups
-  int n_split;          // key-range splits per query block
-  int n_pieces;         // heads * n_split * n_qb
+  // Work units are (head, linear query block), u = head * n_qb + block.  Units
+  // 0 .. n_whole-1 are one piece each (their whole key range, output written
+  // directly); the others are cut into n_split key ranges whose partials the
+  // combine kernel merges.  Pieces: the whole units in order, then the split
+  // pieces ordered (split, unit).
+  int n_whole;
+  int n_split;          // key ranges per split unit (1: every unit is whole)
+  int n_pieces;         // n_whole + (heads * n_qb - n_whole) * n_split
   float scale_log2;     // log2(e) / sqrt(d)
   int n_groups;
   AttnGroup groups[kMaxGroups];

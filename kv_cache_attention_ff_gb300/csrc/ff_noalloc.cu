@@ -127,6 +127,7 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
   ap.heads = heads;
   ff::attn_single_group(ap, nq, nk);
   ap.n_split = split_for(heads * n_qb, ap.groups[0].n_kv, sms);
+  ap.n_whole = ap.n_split > 1 ? 0 : heads * n_qb;  // every unit split, or none
   ap.n_pieces = heads * n_qb * ap.n_split;
   const size_t part_rows = static_cast<size_t>(ap.n_pieces) * 256;
   const size_t need = kErrBytes + part_rows * static_cast<size_t>(head_dim) * 4 + part_rows * 8;
