@@ -173,6 +173,7 @@ int validate_desc(const ff_bank_desc* d) {
   if (T * (2 + (d->history + 1) * d->chunk_frames) > (1ll << 30)) return FF_ERR_ARG;
   if (upf * (d->planner_history + 1) * d->planner_block > (1ll << 31) - 1) return FF_ERR_ARG;
   if (static_cast<long long>(d->heads) * d->head_dim * 2 % 16 != 0) return FF_ERR_ARG;
+  if (upf >= (1ll << 24)) return FF_ERR_ARG;  // the publish kernel's index math is exact below 2^24 units
   return FF_OK;
 }
 
@@ -404,6 +405,8 @@ G1Params publish_params(const ff_bank* b) {
   prm.units_per_row = d.heads * d.head_dim / 8;
   prm.units_per_head = d.head_dim / 8;
   prm.frame_w = d.frame_w;
+  prm.inv_units_per_row = static_cast<float>(1.0 / prm.units_per_row);
+  prm.inv_frame_w = static_cast<float>(1.0 / d.frame_w);
   prm.pt = b->pt;
   prm.py = b->py;
   prm.px = b->px;

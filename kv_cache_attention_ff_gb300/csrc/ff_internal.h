@@ -37,8 +37,10 @@ struct G1Params {
   int y_base, x_base;     // first row-axis and column-axis entries
   long long units_per_frame;  // T * h * d / 8
   int units_per_row;          // h * d / 8  (16-byte units per token)
-  int units_per_head;         // d / 8
+  int units_per_head;         // d / 8 (a power of two)
   int frame_w;
+  float inv_units_per_row;    // fp32 reciprocals for the index divisions
+  float inv_frame_w;
   int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
   int px;
   int n_items;

@@ -73,9 +73,13 @@ __device__ __forceinline__ uint32_t rot_k(float a, float b, float u32, float w32
   const float p1 = __fmul_rn(a, u32);
   const float p2 = __fmul_rn(b, w32);
   const float r = kSub ? __fsub_rn(p1, p2) : __fadd_rn(p1, p2);
-  // |r - exact| <= ~1.5 * 2^-23 (|a u| + |b w|) + 3 * 2^-150; the margin below is 8x that.
+  // |r - exact| <= 3.0001 * 2^-24 * mag: the fp32 cos/sin (2^-24 each), the two
+  // products and the sum/difference (2^-24 each), mag itself within 2^-22 of
+  // |a u| + |b w|, and the contract's own fp64 roundings (~2^-51).  Rounding
+  // r -+ err costs at most another 1.0001 * 2^-24 * mag, so err = 2^-21 * mag
+  // (8 * 2^-24) keeps a factor-two margin; 2^-140 covers subnormal products.
   const float mag = __fadd_rn(fabsf(p1), fabsf(p2));
-  const float err = __fmaf_rn(mag, 0x1p-19f, 0x1p-140f);
+  const float err = __fmaf_rn(mag, 0x1p-21f, 0x1p-140f);
   const uint32_t lo = bf16_bits(__fsub_rn(r, err));
   const uint32_t hi = bf16_bits(__fadd_rn(r, err));
   if (lo == hi && isfinite(r) && isfinite(mag)) return lo;
@@ -110,6 +114,22 @@ __device__ __forceinline__ int rope_index(const G1Params& p, int pair, int t, in
   return p.x_base + x * p.px + pair;
 }
 
+// n / dv for 0 <= n < 2^24, dv >= 1: an fp32 reciprocal estimate (off by at
+// most 2) and an exact integer correction.
+__device__ __forceinline__ int div_small(int n, int dv, float inv) {
+  int q = __float2int_rz(__fmul_rn(__int2float_rn(n), inv));
+  int r = n - q * dv;
+  while (r < 0) {
+    --q;
+    r += dv;
+  }
+  while (r >= dv) {
+    ++q;
+    r -= dv;
+  }
+  return q;
+}
+
 constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 2;
 
@@ -134,10 +154,10 @@ __global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __gr
     const uint4 vin = ld_stream(src_v + off);
     uint4 qin = make_uint4(0, 0, 0, 0);
     if (with_q) qin = ld_stream(q_in + off);
-    const int tok = off / p.units_per_row;
+    const int tok = div_small(off, p.units_per_row, p.inv_units_per_row);
     const int in_row = off - tok * p.units_per_row;
-    const int pair0 = (in_row % p.units_per_head) * 4;
-    const int ty = tok / p.frame_w;
+    const int pair0 = (in_row & (p.units_per_head - 1)) * 4;
+    const int ty = div_small(tok, p.frame_w, p.inv_frame_w);
     const int tx = tok - ty * p.frame_w;
     const uint32_t kw[4] = {kin.x, kin.y, kin.z, kin.w};
     const uint32_t qw[4] = {qin.x, qin.y, qin.z, qin.w};
