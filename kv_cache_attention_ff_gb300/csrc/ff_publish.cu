@@ -60,38 +60,65 @@ __device__ __forceinline__ uint32_t f64_to_bf16_rne(double v) {
   return sign | static_cast<uint32_t>(keep);  // keep == 128 is the smallest normal
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
-}
-
-// One component of a rotated K pair: RNE_bf16(fl64(fl64(a u) -/+ fl64(b w))).
-// u32/w32 are the fp32 roundings of u/w; the fp64 values are fetched only when
-// the fast evaluation cannot decide the rounding.
-// cs points at the fp64 (cos, sin) pair; kSwap selects (u, w) = (sin, cos).
-template <bool kSub, bool kSwap>
-__device__ __forceinline__ uint32_t rot_k(float a, float b, float u32, float w32, const double* cs) {
-  const float p1 = __fmul_rn(a, u32);
-  const float p2 = __fmul_rn(b, w32);
-  const float r = kSub ? __fsub_rn(p1, p2) : __fadd_rn(p1, p2);
-  // |r - exact| <= 3.0001 * 2^-24 * mag: the fp32 cos/sin (2^-24 each), the two
-  // products and the sum/difference (2^-24 each), mag itself within 2^-22 of
-  // |a u| + |b w|, and the contract's own fp64 roundings (~2^-51).  Rounding
-  // r -+ err costs at most another 1.0001 * 2^-24 * mag, so err = 2^-21 * mag
-  // (8 * 2^-24) keeps a factor-two margin; 2^-140 covers subnormal products.
-  const float mag = __fadd_rn(fabsf(p1), fabsf(p2));
-  const float err = __fmaf_rn(mag, 0x1p-21f, 0x1p-140f);
-  const uint32_t lo = bf16_bits(__fsub_rn(r, err));
-  const uint32_t hi = bf16_bits(__fadd_rn(r, err));
-  if (lo == hi && isfinite(r) && isfinite(mag)) return lo;
-  const double u = __ldg(cs + (kSwap ? 1 : 0));
-  const double w = __ldg(cs + (kSwap ? 0 : 1));
-  const double pa = __dmul_rn(static_cast<double>(a), u);
-  const double pb = __dmul_rn(static_cast<double>(b), w);
-  return f64_to_bf16_rne(kSub ? __dsub_rn(pa, pb) : __dadd_rn(pa, pb));
-}
-
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Packed fp32 pairs: (r0, r1) = (a0 * b0, a1 * b1) and (a0 * b0 + c0, a1 * b1 + c1), one rounding each.
+__device__ __forceinline__ void mul2v(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  unsigned long long x, y, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+}
+__device__ __forceinline__ void fma2v(float& r0, float& r1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  unsigned long long x, y, z, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+}
+
+// One rotated K pair, (a', b') = (a c - b s, a s + b c) with c, s the fp64
+// cosine/sine, under the published-K contract; returns a' | b' << 16 (bf16).
+// Fast path in fp32: p = (a c32, a s32), r = (-b s32, b c32) + p with one
+// rounding (fused).  For both components |r - contract| <= 3.0001 * 2^-24 *
+// (|a| + |b|): c32, s32 (2^-24 each), the product, the fused sum and the
+// contract's own fp64 roundings (~2^-51), using |c|, |s| <= 1.  Rounding
+// r -+ err adds at most 1.0001 * 2^-24 * (|a| + |b|), so err = 2^-21 * mag
+// (8 * 2^-24) keeps a factor-two margin; 2^-140 covers subnormal products and
+// mag < 2^126 rules out overflow.  When both ends round to the same bf16 pair
+// that pair is the contract's value; otherwise the fp64 expressions decide.
+__device__ __forceinline__ uint32_t rot_k_pair(uint32_t kw, float2 cs, const double* cs64) {
+  const float a = bf_lo(kw), b = bf_hi(kw);
+  float p0, p1, r0, r1;
+  mul2v(p0, p1, a, a, cs.x, cs.y);
+  fma2v(r0, r1, -b, b, cs.y, cs.x, p0, p1);
+  const float mag = __fadd_rn(fabsf(a), fabsf(b));
+  const float err = __fmaf_rn(mag, 0x1p-21f, 0x1p-140f);
+  float l0, l1, h0, h1;
+  fma2v(h0, h1, err, err, 1.0f, 1.0f, r0, r1);
+  fma2v(l0, l1, err, err, -1.0f, -1.0f, r0, r1);
+  const uint32_t lo = pack_bf16x2(l0, l1), hi = pack_bf16x2(h0, h1);
+  if (lo == hi && mag < 0x1p126f) return lo;
+  const double c = __ldg(cs64), s = __ldg(cs64 + 1);
+  const double ad = static_cast<double>(a), bd = static_cast<double>(b);
+  const uint32_t x = f64_to_bf16_rne(__dsub_rn(__dmul_rn(ad, c), __dmul_rn(bd, s)));
+  const uint32_t y = f64_to_bf16_rne(__dadd_rn(__dmul_rn(ad, s), __dmul_rn(bd, c)));
+  return x | (y << 16);
+}
+
+// One rotated Q pair in fp32 (bf16 out): (qa c - qb s, qa s + qb c).
+__device__ __forceinline__ uint32_t rot_q_pair(uint32_t qw, float2 cs) {
+  const float qa = bf_lo(qw), qb = bf_hi(qw);
+  float p0, p1, r0, r1;
+  mul2v(p0, p1, qa, qa, cs.x, cs.y);
+  fma2v(r0, r1, -qb, qb, cs.y, cs.x, p0, p1);
+  return pack_bf16x2(r0, r1);
+}
+
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 r;
@@ -167,15 +194,8 @@ __global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __gr
       const int idx = rope_index(p, pair0 + e, I.t, ty, tx);
       const float2 cs = __ldg(p.rope32 + idx);
       const double* cs64 = reinterpret_cast<const double*>(p.rope64 + idx);
-      const float a = bf_lo(kw[e]), b = bf_hi(kw[e]);
-      // a' = a c - b s ; b' = a s + b c
-      const uint32_t a2 = rot_k<true, false>(a, b, cs.x, cs.y, cs64);
-      const uint32_t b2 = rot_k<false, true>(a, b, cs.y, cs.x, cs64);
-      ko[e] = a2 | (b2 << 16);
-      const float qa = bf_lo(qw[e]), qb = bf_hi(qw[e]);
-      const float qa2 = __fmaf_rn(qa, cs.x, -__fmul_rn(qb, cs.y));
-      const float qb2 = __fmaf_rn(qa, cs.y, __fmul_rn(qb, cs.x));
-      qo[e] = bf16_bits(qa2) | (bf16_bits(qb2) << 16);
+      ko[e] = rot_k_pair(kw[e], cs, cs64);
+      qo[e] = rot_q_pair(qw[e], cs);
     }
     st_u4(dst_k + off, make_uint4(ko[0], ko[1], ko[2], ko[3]));
     st_u4(dst_v + off, vin);
