@@ -81,28 +81,52 @@ __device__ __forceinline__ void fma2v(float& r0, float& r1, float a0, float a1, 
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
 }
 
+__device__ __forceinline__ void fma2v_rm(float& r0, float& r1, float a0, float a1, float b0, float b1, float c0,
+                                         float c1) {
+  unsigned long long x, y, z, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(c0), "f"(c1));
+  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+}
+__device__ __forceinline__ void fma2v_rp(float& r0, float& r1, float a0, float a1, float b0, float b1, float c0,
+                                         float c1) {
+  unsigned long long x, y, z, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(c0), "f"(c1));
+  asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+}
+
 // One rotated K pair, (a', b') = (a c - b s, a s + b c) with c, s the fp64
 // cosine/sine, under the published-K contract; returns a' | b' << 16 (bf16).
 // Fast path in fp32: p = (a c32, a s32), r = (-b s32, b c32) + p with one
-// rounding (fused).  For both components |r - contract| <= 3.0001 * 2^-24 *
-// (|a| + |b|): c32, s32 (2^-24 each), the product, the fused sum and the
-// contract's own fp64 roundings (~2^-51), using |c|, |s| <= 1.  Rounding
-// r -+ err adds at most 1.0001 * 2^-24 * (|a| + |b|), so err = 2^-21 * mag
-// (8 * 2^-24) keeps a factor-two margin; 2^-140 covers subnormal products and
-// mag < 2^126 rules out overflow.  When both ends round to the same bf16 pair
-// that pair is the contract's value; otherwise the fp64 expressions decide.
+// rounding (fused).  Per component, |r - contract| <= 2^-24 (3 |a||u| +
+// 2 |b||w|) + 2^-51 (|a||u| + |b||w|) <= 3.0002 * 2^-24 * m, where (u, w) is
+// (c, s) or (s, c) and m = |a||u32| + |b||w32| as computed (the fp32 cos/sin,
+// the product and the fused sum each cost 2^-24; the contract's own fp64
+// roundings ~2^-52; m itself is within 2^-22 of the exact magnitude).  The
+// interval ends r -+ err are rounded outward, err = 2^-22 m + 2^-140 rounded
+// up (4 * 2^-24 * m; 2^-140 covers subnormal products; m < 2^126 rules out
+// overflow and NaN).  When both ends round to the same bf16 pair that pair
+// is the contract's value; otherwise the fp64 expressions decide.
 __device__ __forceinline__ uint32_t rot_k_pair(uint32_t kw, float2 cs, const double* cs64) {
   const float a = bf_lo(kw), b = bf_hi(kw);
   float p0, p1, r0, r1;
   mul2v(p0, p1, a, a, cs.x, cs.y);
   fma2v(r0, r1, -b, b, cs.y, cs.x, p0, p1);
-  const float mag = __fadd_rn(fabsf(a), fabsf(b));
-  const float err = __fmaf_rn(mag, 0x1p-21f, 0x1p-140f);
+  const float aa = fabsf(a), ab = fabsf(b), ac = fabsf(cs.x), as = fabsf(cs.y);
+  float m0, m1, e0, e1;
+  mul2v(m0, m1, ab, ab, as, ac);
+  fma2v_rp(m0, m1, aa, aa, ac, as, m0, m1);
+  fma2v_rp(e0, e1, m0, m1, 0x1p-22f, 0x1p-22f, 0x1p-140f, 0x1p-140f);
   float l0, l1, h0, h1;
-  fma2v(h0, h1, err, err, 1.0f, 1.0f, r0, r1);
-  fma2v(l0, l1, err, err, -1.0f, -1.0f, r0, r1);
+  fma2v_rm(l0, l1, e0, e1, -1.0f, -1.0f, r0, r1);
+  fma2v_rp(h0, h1, e0, e1, 1.0f, 1.0f, r0, r1);
   const uint32_t lo = pack_bf16x2(l0, l1), hi = pack_bf16x2(h0, h1);
-  if (lo == hi && mag < 0x1p126f) return lo;
+  if (lo == hi && m0 < 0x1p126f && m1 < 0x1p126f) return lo;  // false for NaN inputs
   const double c = __ldg(cs64), s = __ldg(cs64 + 1);
   const double ad = static_cast<double>(a), bd = static_cast<double>(b);
   const uint32_t x = f64_to_bf16_rne(__dsub_rn(__dmul_rn(ad, c), __dmul_rn(bd, s)));
