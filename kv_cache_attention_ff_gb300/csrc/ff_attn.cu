@@ -71,7 +71,8 @@ struct Piece {
   int head, g, qb, kv0, kv1, part;
 };
 
-__device__ __forceinline__ Piece decode_piece(const AttnParams& p, int piece) {
+template <class P>
+__device__ __forceinline__ Piece decode_piece(const P& p, int piece) {
   Piece r;
   int unit, split, ns;
   if (piece < p.n_whole) {
@@ -131,10 +132,10 @@ struct TileCursor {
   }
 };
 
-template <int D>
+template <int D, class P>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ KVMaps kv,
-                     const __grid_constant__ AttnParams p) {
+                     const __grid_constant__ P p) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -486,8 +487,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // Merge the key-range pieces of each (head, query block): with per-piece
 // running max m_s (log2 units), sum l_s and unnormalised O_s,
 //   m = max m_s,  l = sum l_s 2^(m_s - m),  O = sum O_s 2^(m_s - m) / l.
-template <int D>
-__global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+template <int D, class P>
+__global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_constant__ P p) {
   constexpr int PER = D / 8;  // elements per thread
   const int rest = p.heads * p.n_qb - p.n_whole;  // split units
   const int ru = blockIdx.x;                       // index among the split units
@@ -544,28 +545,63 @@ size_t attention_smem_bytes(int head_dim) {
 
 cudaError_t attention_configure(int head_dim) {
   cudaError_t e;
-  if (head_dim == 128)
-    e = cudaFuncSetAttribute(bank_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<128>::SMEM);
-  else
-    e = cudaFuncSetAttribute(bank_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<64>::SMEM);
+  if (head_dim == 128) {
+    e = cudaFuncSetAttribute(bank_attn_kernel<128, AttnParamsN<1>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnCfg<128>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bank_attn_kernel<128, AttnParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AttnCfg<128>::SMEM);
+  } else {
+    e = cudaFuncSetAttribute(bank_attn_kernel<64, AttnParamsN<1>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnCfg<64>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bank_attn_kernel<64, AttnParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AttnCfg<64>::SMEM);
+  }
   return e;
 }
 
+namespace {
+// A copy of `p` sized for its single query group.
+AttnParamsN<1> single_group(const AttnParams& p) {
+  AttnParamsN<1> q{};
+  static_cast<AttnHeader&>(q) = p;
+  q.groups[0] = p.groups[0];
+  return q;
+}
+}  // namespace
+
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& kv, const AttnParams& p, int grid,
                              cudaStream_t s) {
-  if (head_dim == 128)
-    bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, p);
-  else
-    bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
+  if (p.n_groups == 1) {
+    const AttnParamsN<1> q = single_group(p);
+    if (head_dim == 128)
+      bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, q);
+    else
+      bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, q);
+  } else {
+    if (head_dim == 128)
+      bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, p);
+    else
+      bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
   dim3 grid(p.heads * p.n_qb - p.n_whole, 16);  // split units; 16 rows x 8 parts per 128-thread block
-  if (head_dim == 128)
-    attn_combine_kernel<128><<<grid, 128, 0, s>>>(p);
-  else
-    attn_combine_kernel<64><<<grid, 128, 0, s>>>(p);
+  if (p.n_groups == 1) {
+    const AttnParamsN<1> q = single_group(p);
+    if (head_dim == 128)
+      attn_combine_kernel<128><<<grid, 128, 0, s>>>(q);
+    else
+      attn_combine_kernel<64><<<grid, 128, 0, s>>>(q);
+  } else {
+    if (head_dim == 128)
+      attn_combine_kernel<128><<<grid, 128, 0, s>>>(p);
+    else
+      attn_combine_kernel<64><<<grid, 128, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -28,8 +28,9 @@ struct G1Item {
 };
 
 constexpr int kMaxItems = 160;
+constexpr int kFewItems = 8;  // launches with at most this many items use a small parameter block
 
-struct G1Params {
+struct G1Header {
   const void* q_in;   // [F * T, h, d] queries before rotary encoding (or null)
   void* q_rot;        // [F * T, h, d]
   const double2* rope64;  // rotary (cos, sin) in fp64: [total_frames][pt], then [frame_h][py], then [frame_w][px]
@@ -44,8 +45,13 @@ struct G1Params {
   int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
   int px;
   int n_items;
-  G1Item items[kMaxItems];
 };
+
+template <int N>
+struct G1ParamsN : G1Header {
+  G1Item items[N];
+};
+using G1Params = G1ParamsN<kMaxItems>;
 
 // ----------------------------------------------------------------- attention
 
@@ -79,7 +85,7 @@ struct KVMaps {
   CUtensorMap v[kMaxMaps];
 };
 
-struct AttnParams {
+struct AttnHeader {
   void* out;            // bf16 [query rows, h, d]
   float* part_o;        // [split pieces][256][d] unnormalised partial outputs
   float* part_ml;       // [split pieces][256][2] running max (log2 units) and sum
@@ -96,8 +102,16 @@ struct AttnParams {
   int n_pieces;         // n_whole + (heads * n_qb - n_whole) * n_split
   float scale_log2;     // log2(e) / sqrt(d)
   int n_groups;
-  AttnGroup groups[kMaxGroups];
 };
+
+// Kernel parameters with room for NG query groups; launches with one group
+// (every renderer and planner call) use NG = 1, which keeps the parameter
+// block small.
+template <int NG>
+struct AttnParamsN : AttnHeader {
+  AttnGroup groups[NG];
+};
+using AttnParams = AttnParamsN<kMaxGroups>;
 
 // Fill `p` with the single group [0, nq) x one key segment [0, nk) of map 0.
 inline void attn_single_group(AttnParams& p, int nq, int nk) {

@@ -157,7 +157,7 @@ __device__ __forceinline__ void st_u4(void* p, uint4 v) {
 
 // Index of channel pair `pair` for a token at (t, y, x) in the rotary tables
 // (time rows, then row-axis rows, then column-axis rows).
-__device__ __forceinline__ int rope_index(const G1Params& p, int pair, int t, int y, int x) {
+__device__ __forceinline__ int rope_index(const G1Header& p, int pair, int t, int y, int x) {
   if (pair < p.pt) return t * p.pt + pair;
   pair -= p.pt;
   if (pair < p.py) return p.y_base + y * p.py + pair;
@@ -184,7 +184,8 @@ __device__ __forceinline__ int div_small(int n, int dv, float inv) {
 constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 2;
 
-__global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __grid_constant__ G1Params p) {
+template <int N>
+__global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
   const uint4* src_k = static_cast<const uint4*>(I.src_k);
@@ -230,7 +231,14 @@ __global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __gr
 cudaError_t launch_publish(const G1Params& p, int /*grid_hint*/, cudaStream_t s) {
   const int upf = static_cast<int>(p.units_per_frame);
   dim3 grid((upf + kPubThreads * kPubUnroll - 1) / (kPubThreads * kPubUnroll), p.n_items);
-  rope_publish_kernel<<<grid, kPubThreads, 0, s>>>(p);
+  if (p.n_items <= kFewItems) {
+    G1ParamsN<kFewItems> q{};
+    static_cast<G1Header&>(q) = p;
+    for (int i = 0; i < p.n_items; ++i) q.items[i] = p.items[i];
+    rope_publish_kernel<kFewItems><<<grid, kPubThreads, 0, s>>>(q);
+  } else {
+    rope_publish_kernel<kMaxItems><<<grid, kPubThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
