@@ -182,7 +182,7 @@ __device__ __forceinline__ int div_small(int n, int dv, float inv) {
 }
 
 constexpr int kPubThreads = 128;
-constexpr int kPubUnroll = 2;
+constexpr int kPubUnroll = 1;
 
 template <int N>
 __global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
