@@ -42,6 +42,11 @@ def _bf16_of_f32(x):
 
 def fast_path(a, b, c64, s64):
     """Returns (accepted mask, bf16 bits of the two components) of the fp32 path."""
+    with np.errstate(over="ignore", invalid="ignore"):  # special inputs overflow or are NaN by design
+        return _fast_path(a, b, c64, s64)
+
+
+def _fast_path(a, b, c64, s64):
     c32, s32 = c64.astype(np.float32), s64.astype(np.float32)
     r0 = _fma(-b, s32, _mul(a, c32))
     r1 = _fma(b, c32, _mul(a, s32))
@@ -52,8 +57,7 @@ def fast_path(a, b, c64, s64):
     e1 = _fma(m1, np.float32(2.0 ** -22), np.float32(2.0 ** -140), "up")
     lo0, hi0 = _bf16_of_f32(_fma(e0, -1, r0, "down")), _bf16_of_f32(_fma(e0, 1, r0, "up"))
     lo1, hi1 = _bf16_of_f32(_fma(e1, -1, r1, "down")), _bf16_of_f32(_fma(e1, 1, r1, "up"))
-    with np.errstate(invalid="ignore"):
-        ok = (lo0 == hi0) & (lo1 == hi1) & (m0 < 2.0 ** 126) & (m1 < 2.0 ** 126)
+    ok = (lo0 == hi0) & (lo1 == hi1) & (m0 < 2.0 ** 126) & (m1 < 2.0 ** 126)
     return ok, lo0, lo1
 
 
