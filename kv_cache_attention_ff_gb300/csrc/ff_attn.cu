@@ -487,9 +487,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // Merge the key-range pieces of each (head, query block): with per-piece
 // running max m_s (log2 units), sum l_s and unnormalised O_s,
 //   m = max m_s,  l = sum l_s 2^(m_s - m),  O = sum O_s 2^(m_s - m) / l.
+// One thread per 8 output columns of a row; it issues the loads of all pieces
+// before the first use, so the merge costs one round trip to L2.
+constexpr int kCombineThreads = 128;
+
 template <int D, class P>
-__global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_constant__ P p) {
-  constexpr int PER = D / 8;  // elements per thread
+__global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const __grid_constant__ P p) {
+  constexpr int PER = 8;                           // columns per thread
+  constexpr int TPR = D / PER;                     // threads per row
+  constexpr int ROWS = kCombineThreads / TPR;      // rows per block
   const int rest = p.heads * p.n_qb - p.n_whole;  // split units
   const int ru = blockIdx.x;                       // index among the split units
   const int unit = p.n_whole + ru;                 // head * n_qb + linear query block
@@ -499,34 +505,45 @@ __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_const
   while (g + 1 < p.n_groups && p.groups[g + 1].qb0 <= lin) ++g;
   const AttnGroup& G = p.groups[g];
   const int qb = lin - G.qb0;
-  const int rloc = blockIdx.y * 16 + (threadIdx.x >> 3);  // 0..255
-  const int part = threadIdx.x & 7;
+  const int rloc = blockIdx.y * ROWS + threadIdx.x / TPR;  // 0..255
+  const int part = threadIdx.x % TPR;
   const int lrow = qb * 256 + rloc;
   if (lrow >= G.nq) return;
   const int row = G.q_row0 + lrow;
+  const int ns = p.n_split;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  float m = -INFINITY;
-  for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = static_cast<size_t>(s) * rest + ru;
-    m = fmaxf(m, ml[piece * 256 + rloc].x);
+  float2 mls[kMaxSplit];
+  float4 os[kMaxSplit][PER / 4];
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < ns) {
+      const size_t piece = static_cast<size_t>(s) * rest + ru;
+      mls[s] = ml[piece * 256 + rloc];
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + (piece * 256 + rloc) * D + part * PER);
+#pragma unroll
+      for (int i = 0; i < PER / 4; ++i) os[s][i] = src[i];
+    }
   }
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s)
+    if (s < ns) m = fmaxf(m, mls[s].x);
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
-    const size_t piece = static_cast<size_t>(s) * rest + ru;
-    const float2 v = ml[piece * 256 + rloc];
-    const float w = exp2f(v.x - m);
-    l = __fmaf_rn(v.y, w, l);
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + (piece * 256 + rloc) * D + part * PER);
 #pragma unroll
-    for (int i = 0; i < PER / 4; ++i) {
-      const float4 o = src[i];
-      acc[4 * i] = __fmaf_rn(o.x, w, acc[4 * i]);
-      acc[4 * i + 1] = __fmaf_rn(o.y, w, acc[4 * i + 1]);
-      acc[4 * i + 2] = __fmaf_rn(o.z, w, acc[4 * i + 2]);
-      acc[4 * i + 3] = __fmaf_rn(o.w, w, acc[4 * i + 3]);
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < ns) {
+      const float w = exp2f(mls[s].x - m);
+      l = __fmaf_rn(mls[s].y, w, l);
+#pragma unroll
+      for (int i = 0; i < PER / 4; ++i) {
+        acc[4 * i] = __fmaf_rn(os[s][i].x, w, acc[4 * i]);
+        acc[4 * i + 1] = __fmaf_rn(os[s][i].y, w, acc[4 * i + 1]);
+        acc[4 * i + 2] = __fmaf_rn(os[s][i].z, w, acc[4 * i + 2]);
+        acc[4 * i + 3] = __fmaf_rn(os[s][i].w, w, acc[4 * i + 3]);
+      }
     }
   }
   const float inv = 1.0f / l;
@@ -534,9 +551,7 @@ __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const __grid_const
   uint32_t w[PER / 2];
 #pragma unroll
   for (int i = 0; i < PER / 2; ++i) w[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-#pragma unroll
-  for (int i = 0; i < PER / 8; ++i)
-    reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 size_t attention_smem_bytes(int head_dim) {
@@ -589,18 +604,19 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& 
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
-  dim3 grid(p.heads * p.n_qb - p.n_whole, 16);  // split units; 16 rows x 8 parts per 128-thread block
+  // split units x 256 rows in blocks of 128 / (d / 8) rows
+  dim3 grid(p.heads * p.n_qb - p.n_whole, 256 / (kCombineThreads / (head_dim / 8)));
   if (p.n_groups == 1) {
     const AttnParamsN<1> q = single_group(p);
     if (head_dim == 128)
-      attn_combine_kernel<128><<<grid, 128, 0, s>>>(q);
+      attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(q);
     else
-      attn_combine_kernel<64><<<grid, 128, 0, s>>>(q);
+      attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(q);
   } else {
     if (head_dim == 128)
-      attn_combine_kernel<128><<<grid, 128, 0, s>>>(p);
+      attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
     else
-      attn_combine_kernel<64><<<grid, 128, 0, s>>>(p);
+      attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

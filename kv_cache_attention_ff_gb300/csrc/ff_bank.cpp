@@ -232,7 +232,7 @@ SplitPlan plan_split(int units, int n_kv, int sms, size_t max_part_rows) {
   SplitPlan best{units, 1, units, 0};
   double best_cost = 1e300;
   std::vector<double> load(static_cast<size_t>(std::max(sms, 1)));
-  for (int ns = 1; ns <= std::min(4, n_kv); ++ns) {
+  for (int ns = 1; ns <= std::min(kMaxSplit, n_kv); ++ns) {
     for (int m = 0; m * sms <= units; ++m) {
       const int n_whole = (ns == 1) ? units : m * sms;
       const int rest = units - n_whole;

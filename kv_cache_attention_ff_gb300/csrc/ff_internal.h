@@ -66,6 +66,7 @@ using G1Params = G1ParamsN<kMaxItems>;
 constexpr int kMaxGroups = 96;
 constexpr int kMaxSegs = 4;
 constexpr int kMaxMaps = 4;
+constexpr int kMaxSplit = 4;  // key ranges a split unit is cut into, at most
 
 struct AttnGroup {
   int q_row0;              // first query row of the group

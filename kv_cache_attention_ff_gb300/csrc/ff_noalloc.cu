@@ -48,7 +48,7 @@ int split_for(int units, int n_kv, int sms) {
   if (n_kv < 2) return 1;
   double best = 1e300;
   int best_s = 2;
-  for (int s = 2; s <= (n_kv < 4 ? n_kv : 4); ++s) {
+  for (int s = 2; s <= (n_kv < ff::kMaxSplit ? n_kv : ff::kMaxSplit); ++s) {
     const long long pieces = static_cast<long long>(units) * s;
     const long long waves = (pieces + sms - 1) / sms;
     const double cost = static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0);

@@ -185,7 +185,7 @@ constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 1;
 
 template <int N>
-__global__ void __launch_bounds__(kPubThreads, 8) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
+__global__ void __launch_bounds__(kPubThreads, 12) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
   const uint4* src_k = static_cast<const uint4*>(I.src_k);
