@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
 # a kernel edited since then reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (220.2e6, "ff_attn.cu", "765c7d9da16b1f0c"),
-    "rope_publish_kernel": (45.4e6, "ff_publish.cu", "7aeed142d5f1e347"),
+    "bank_attn_kernel": (221.1e6, "ff_attn.cu", "16db896386b0d636"),
+    "rope_publish_kernel": (45.4e6, "ff_publish.cu", "8d7c319d83a01424"),
 }
 
 
