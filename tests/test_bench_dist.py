@@ -49,3 +49,38 @@ def test_single_rank_aggregate():
     import bench
     ms, value = bench.aggregate(5.0, 1e12, 1)
     assert ms == 5.0 and value == pytest.approx(200.0)
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _clock_line(t, sm, power_cap):
+    import datetime
+    ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    cap = "Active" if power_cap else "Not Active"
+    return f"{ts}, 0, {sm}, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+
+
+def test_clock_summary_keeps_samples_inside_the_timed_window():
+    sys.path.insert(0, ROOT)
+    import time
+
+    import bench
+    now = time.time()
+    c = bench.ClockSampler(0)
+    c.proc = _DoneProc()
+    c.lines = [_clock_line(now - 2.0, 2070, False), _clock_line(now, 1900, True), _clock_line(now + 0.05, 1910, True),
+               _clock_line(now + 3.0, 2070, False), "garbage line"]
+    c.mark(now - 0.01, now + 0.06)
+    r = c.stop()
+    assert r["window"] == "timed window" and r["samples"] == 2
+    assert r["sm_mhz"] == 1905.0 and r["sm_max_mhz"] == 2070.0 and r["reasons"] == ["sw_power_cap"]
+    # no sample inside the window: the summary falls back to every sample and says so
+    c.mark(now + 10.0, now + 11.0)
+    r = c.stop()
+    assert r["samples"] == 4 and r["window"].startswith("all samples")
