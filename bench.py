@@ -603,9 +603,45 @@ def cpu_baseline(budget_s: float = 15.0):
     heads = int(min(12, max(1, budget_s * rate // per_head)))
     rows = 4680 if heads > 1 else int(min(4680, max(128, budget_s * rate / (4.0 * 31200 * 128))))
     dt, fl = oracle_sample(rows, heads, seed=1)
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
+    rate = fl / dt
+    tiny_s, tiny_fl = oracle_tiny_bruteforce()
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
             "sample": f"fp64 numpy oracle attention of {rows} query rows x {heads} heads over the 31200 keys of "
-                      f"the steady 1.3B call ({fl / 1e9:.1f} GFLOP, {dt:.1f} s); rope/publish/gather not included"}
+                      f"the steady 1.3B call ({fl / 1e9:.1f} GFLOP, {dt:.1f} s); rope/publish/gather not included",
+            "cpu_count": os.cpu_count(), "affinity": _host_cores(), "blas_threads": _blas_threads(),
+            "chunk_steps_per_s": round(rate / (30 * 4.0 * 4680 * 31200 * 128 * 12), 6),
+            "tiny_bruteforce": {"seconds": round(tiny_s, 3), "gflops": round(tiny_fl / tiny_s / 1e9, 6), "cores": 1,
+                                "sample": "pure-Python attention of the tiny schedule's chunk 2 "
+                                          "(48 queries x 176 keys x 2 heads, d 64)"}}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return f"{var}={os.environ[var]}"
+    return "library default (threadpoolctl unavailable)"
+
+
+def oracle_tiny_bruteforce():
+    """Time the oracle's pure-Python attention on one call of the tiny schedule
+    (chunk 2: 48 queries over 176 keys, 2 heads, d 64) on one core."""
+    import numpy as np
+
+    from oracle import ff_oracle as fo
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((48, 2, 64)).tolist()
+    k = rng.standard_normal((176, 2, 64)).tolist()
+    v = rng.standard_normal((176, 2, 64)).tolist()
+    t0 = time.perf_counter()
+    fo.attention_bruteforce(q, k, v)
+    return time.perf_counter() - t0, 4.0 * 48 * 176 * 64 * 2
 
 
 def run_reference(args):
