@@ -319,6 +319,7 @@ def run_gpu(args):
 
     planner = None if args.no_e2e else run_planner(stream, args, dev)
     packed = None if args.no_e2e else run_packed(stream, args, dev)
+    schedule = None if args.no_e2e else run_schedule(pool, stream, args, dev)
     baselines = None if args.no_e2e else run_baselines(pool, stream, args, dev, flops)
 
     cpu = None
@@ -340,7 +341,7 @@ def run_gpu(args):
             "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "packed": packed, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -443,6 +444,52 @@ def run_baselines(pool, stream, args, dev, flops):
     res["note"] = ("attention calls only, one layer, one GPU, S=4 stages; the pages report 1.42-2.92x vs "
                    "Self-Forcing and 1.16-1.69x vs HiAR end to end with up to 4 GPUs")
     return res
+
+
+def run_schedule(pool, stream, args, dev):
+    """The full 81-latent schedule of the 1.3B 480p shape on one GPU: anchors
+    published first (3 planner blocks of 3 per layer), then 27 chunks x 4 stages
+    x 30 layers of renderer calls in chunk-step order (chunk i, stage k, all
+    layers), ramp-up chunks included.  Inputs cycle the pool (time does not
+    depend on values)."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff, synth
+    T, H, D, L, N = 1560, 12, 128, 30, 81
+    sb = ff.Bank(n_layers=L, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                 total_frames=N, heads=H, head_dim=D, frame_h=30, frame_w=52, device=dev.index)
+    with torch.cuda.stream(stream):
+        ka = synth.device_frames(2, 0, synth.ANCHOR_STREAM, synth.K, list(range(0, N, 10)), T, H, D, "ar", device=dev)
+        va = synth.device_frames(2, 0, synth.ANCHOR_STREAM, synth.V, list(range(0, N, 10)), T, H, D, "normal",
+                                 device=dev)
+        blocks = [(ka[3 * b * T:3 * (b + 1) * T].contiguous(), va[3 * b * T:3 * (b + 1) * T].contiguous())
+                  for b in range(3)]
+        out = torch.empty((3 * T, H, D), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record(stream)
+    for layer in range(L):
+        for b in range(3):
+            sb.anchor_publish(layer, 30 * b, 3, blocks[b][0], blocks[b][1], stream)
+    e1.record(stream)
+    for i in range(27):
+        for st in range(4):
+            q, k, v = pool[st][i % 4]
+            for layer in range(L):
+                sb.render_attn(layer, st, i, q, k, v, out, stream)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    assert sb.error_poll() == 0
+    key_frames = 0
+    for i in range(27):
+        key_frames += len(sb.gamma(i)) + 3 * min(i, 5) + 3
+    sb.close()
+    render_s = e1.elapsed_time(e2) / 1e3
+    flops = 4.0 * (3 * T) * (key_frames * T) * D * H * 4 * L
+    return {"workload": "1.3B 480p full schedule: 27 chunks x 4 stages x 30 layers, anchors published first",
+            "renderer_calls": 27 * 4 * L, "key_frames_per_layer_stage": key_frames,
+            "anchor_publish_ms": round(e0.elapsed_time(e1), 3), "render_ms": round(1e3 * render_s, 2),
+            "chunk_steps_per_s": round(27 * 4 / render_s, 2), "tflops": round(flops / render_s / 1e12, 1)}
 
 
 def run_packed(stream, args, dev):
