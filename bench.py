@@ -320,6 +320,12 @@ def run_gpu(args):
     planner = None if args.no_e2e else run_planner(stream, args, dev)
     packed = None if args.no_e2e else run_packed(stream, args, dev)
     schedule = None if args.no_e2e else run_schedule(pool, stream, args, dev)
+    configs = None
+    if not args.no_e2e:
+        try:
+            configs = run_configs(stream, args, dev)
+        except Exception as exc:  # an extra measurement must not lose the line
+            configs = {"error": f"{type(exc).__name__}: {exc}"}
     baselines = None if args.no_e2e else run_baselines(pool, stream, args, dev, flops)
 
     cpu = None
@@ -341,7 +347,7 @@ def run_gpu(args):
             "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -490,6 +496,65 @@ def run_schedule(pool, stream, args, dev):
             "renderer_calls": 27 * 4 * L, "key_frames_per_layer_stage": key_frames,
             "anchor_publish_ms": round(e0.elapsed_time(e1), 3), "render_ms": round(1e3 * render_s, 2),
             "chunk_steps_per_s": round(27 * 4 / render_s, 2), "tflops": round(flops / render_s / 1e12, 1)}
+
+
+def run_configs(stream, args, dev):
+    """Steady renderer calls of the 14B shapes (40 heads, d 128): 480p (4680 queries
+    over 31200 keys) and the 720p long rollout (10800 queries over 72000 keys, 261
+    latents, 6 anchor slots filled on demand).  One layer and one stage: a call's
+    work does not depend on them.  The timed chunks are steady chunks whose anchors
+    all stay resident (720p: chunks 8..16, anchor blocks 0 and 1 in the 6-slot
+    ring)."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff, synth
+    res = {}
+    for name, cfg_id, fh, fw, N, cap, reps in (("wan14b_480p", 4, 30, 52, 81, 9, 18),
+                                               ("wan14b_720p", 5, 45, 80, 261, 6, 9)):
+        T, H, D = fh * fw, 40, 128
+        cb = ff.Bank(n_layers=1, n_stages=1, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=cap,
+                     total_frames=N, heads=H, head_dim=D, frame_h=fh, frame_w=fw, device=dev.index)
+        with torch.cuda.stream(stream):
+            q, k = (synth.device_frames(cfg_id, 0, 0, t, [0, 1, 2], T, H, D, "ar", device=dev) for t in (0, 1))
+            v = synth.device_frames(cfg_id, 0, 0, 2, [0, 1, 2], T, H, D, "normal", device=dev)
+            out = torch.empty_like(q)
+        published = set()
+
+        def publish_for(i):
+            for a in cb.gamma(i):
+                blk = a // 30
+                if blk in published:
+                    continue
+                frames = [f for f in (30 * blk, 30 * blk + 10, 30 * blk + 20) if f < N]
+                with torch.cuda.stream(stream):
+                    ak = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.K, frames, T, H, D, "ar", device=dev)
+                    av = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.V, frames, T, H, D, "normal",
+                                             device=dev)
+                cb.anchor_publish(0, 30 * blk, len(frames), ak, av, stream)
+                published.add(blk)
+
+        first = 5 + 3  # ramp-up chunks 0..4 and 3 warm-up calls untimed
+        for i in range(first):
+            publish_for(i)
+            cb.render_attn(0, 0, i, q, k, v, out, stream)
+        for i in range(first, first + reps):  # anchors of the timed chunks, before timing
+            publish_for(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(first, first + reps):
+            cb.render_attn(0, 0, i, q, k, v, out, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert cb.error_poll() == 0
+        key_frames = [len(cb.gamma(i)) + 15 + 3 for i in range(first, first + reps)]
+        cb.close()
+        ms = e0.elapsed_time(e1) / reps
+        flops = sum(4.0 * (3 * T) * (kf * T) * D * H for kf in key_frames) / reps
+        res[name] = {"queries": 3 * T, "keys": key_frames[0] * T, "heads": H, "calls": reps,
+                     "tflop_per_call": round(flops / 1e12, 3), "ms_per_call": round(ms, 3),
+                     "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+    return res
 
 
 def run_packed(stream, args, dev):
