@@ -183,9 +183,13 @@ __device__ __forceinline__ int div_small(int n, int dv, float inv) {
 
 constexpr int kPubThreads = 128;
 constexpr int kPubUnroll = 1;
+// The kernel mostly waits on its loads, so it is compiled for 12 resident
+// blocks per SM (48 warps, at most 40 registers); 10 blocks at 48 registers
+// and 16 blocks at 32 registers (with spills) were both slower.
+constexpr int kPubMinBlocks = 12;
 
 template <int N>
-__global__ void __launch_bounds__(kPubThreads, 12) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
+__global__ void __launch_bounds__(kPubThreads, kPubMinBlocks) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
   const uint4* src_k = static_cast<const uint4*>(I.src_k);
