@@ -575,7 +575,7 @@ def run_packed(stream, args, dev):
         ws = torch.empty(pb.packed_workspace_bytes(), dtype=torch.uint8, device=dev)
         out = torch.empty_like(q)
     torch.cuda.synchronize()
-    reps = max(3, args.steps // 4)
+    reps = max(3, min(50, args.steps // 4))
     for _ in range(2):
         pb.packed_render_attn(q, k, v, ak, av, out, ws, stream)
     torch.cuda.synchronize()
@@ -763,7 +763,7 @@ def run_reference(args):
     dt0, f0 = oracle_sample(64, 1)
     rate = f0 / max(dt0, 1e-6)
     # each step: a bounded sample sized so that all steps take about a minute
-    per_step_s = max(0.25, 60.0 / max(args.steps + args.warmup, 1))
+    per_step_s = max(0.05, 60.0 / max(args.steps + args.warmup, 1))
     rows = int(min(4680, max(16, per_step_s * rate / (4.0 * 31200 * 128))))
     times, fl = [], 0.0
     for j in range(args.warmup + args.steps):
@@ -789,12 +789,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--clock-ms", type=int, default=100, help="nvidia-smi sampling interval during the timed region")
+    ap.add_argument("--clock-ms", type=int, default=50, help="nvidia-smi sampling interval during the timed region")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass (profiling runs)")
     ap.add_argument("--stage-streams", type=int, default=1,
                     help="CUDA streams the 4 stages are issued on (1..4); per-kernel event times need 1")

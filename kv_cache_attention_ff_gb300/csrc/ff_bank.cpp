@@ -405,7 +405,6 @@ G1Params publish_params(const ff_bank* b) {
   prm.units_per_row = d.heads * d.head_dim / 8;
   prm.units_per_head = d.head_dim / 8;
   prm.frame_w = d.frame_w;
-  prm.inv_units_per_row = static_cast<float>(1.0 / prm.units_per_row);
   prm.inv_frame_w = static_cast<float>(1.0 / d.frame_w);
   prm.pt = b->pt;
   prm.py = b->py;

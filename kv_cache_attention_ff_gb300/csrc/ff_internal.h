@@ -12,7 +12,8 @@ namespace ff {
 // One launch of the RoPE + publish kernel processes a list of frame-sized work
 // items.  Every item covers one latent frame of one (K, V) pair,
 // T * heads * head_dim bf16 each, split into 16-byte units; a thread handles
-// the same unit offset of whatever an item touches.  An item reads a K and a V
+// the same unit offsets of whatever an item touches (one unit of G consecutive
+// heads of a token, sharing their rotary angles).  An item reads a K and a V
 // frame, rotates K under the published-K contract and writes both to their
 // destination frames (a stage-ring slot, an anchor slot or a scratch buffer);
 // with q_frame >= 0 it also rotates frame q_frame of the Q input into the same
@@ -40,8 +41,7 @@ struct G1Header {
   int units_per_row;          // h * d / 8  (16-byte units per token)
   int units_per_head;         // d / 8 (a power of two)
   int frame_w;
-  float inv_units_per_row;    // fp32 reciprocals for the index divisions
-  float inv_frame_w;
+  float inv_frame_w;          // fp32 reciprocal for the token -> (row, column) division
   int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
   int px;
   int n_items;
@@ -49,6 +49,7 @@ struct G1Header {
 
 template <int N>
 struct G1ParamsN : G1Header {
+  static constexpr int kItems = N;
   G1Item items[N];
 };
 using G1Params = G1ParamsN<kMaxItems>;

@@ -25,6 +25,10 @@
 #include "ff_internal.h"
 #include "ff_ptx.cuh"
 
+#ifndef FF_PUB_G
+#define FF_PUB_G 2
+#endif
+
 namespace ff {
 
 // fp64 -> bf16 with one round-to-nearest-even, from the binary64 bit fields.
@@ -182,16 +186,26 @@ __device__ __forceinline__ int div_small(int n, int dv, float inv) {
 }
 
 constexpr int kPubThreads = 128;
-constexpr int kPubUnroll = 1;
-// The kernel mostly waits on its loads, so it is compiled for 12 resident
-// blocks per SM (48 warps, at most 40 registers); 10 blocks at 48 registers
-// and 16 blocks at 32 registers (with spills) were both slower.
-constexpr int kPubMinBlocks = 12;
 
-template <int N>
-__global__ void __launch_bounds__(kPubThreads, kPubMinBlocks) rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
+// Resident blocks per SM the kernel is compiled for, by heads per thread: it
+// mostly waits on its loads, so occupancy is traded against registers.
+template <int G>
+struct PubBounds {
+  static constexpr int kMinBlocks = G == 1 ? 12 : (G == 2 ? 8 : 6);
+};
+
+// A thread rotates and stores the same 16-byte unit (8 channels, 4 pairs) of
+// G consecutive heads of one token: the token's position, the rotary table
+// entries and the index arithmetic are shared by the G units.  Lanes run over
+// the units of a head first, so each load instruction of a warp covers whole
+// 128- or 256-byte head rows.
+template <int N, int G>
+__global__ void __launch_bounds__(kPubThreads, PubBounds<G>::kMinBlocks)
+    rope_publish_kernel(const __grid_constant__ G1ParamsN<N> p) {
   const G1Item& I = p.items[blockIdx.y];
   const int upf = static_cast<int>(p.units_per_frame);
+  const int tid = blockIdx.x * kPubThreads + threadIdx.x;
+  if (tid >= upf / G) return;
   const uint4* src_k = static_cast<const uint4*>(I.src_k);
   const uint4* src_v = static_cast<const uint4*>(I.src_v);
   uint4* dst_k = static_cast<uint4*>(I.dst_k);
@@ -201,47 +215,73 @@ __global__ void __launch_bounds__(kPubThreads, kPubMinBlocks) rope_publish_kerne
   const uint4* q_in = static_cast<const uint4*>(p.q_in) + q_base;
   uint4* q_out = static_cast<uint4*>(p.q_rot) + q_base;
 
-  const int base = blockIdx.x * (kPubThreads * kPubUnroll) + threadIdx.x;
+  const int uph = p.units_per_head;             // a power of two
+  const int groups = p.units_per_row / (uph * G);  // head groups per token
+  const int o = tid & (uph - 1);
+  const int rest = tid >> (__ffs(uph) - 1);
+  const int tok = rest / groups;
+  const int off0 = tok * p.units_per_row + (rest - tok * groups) * (G * uph) + o;
+  uint4 kin[G], vin[G], qin[G];
 #pragma unroll
-  for (int j = 0; j < kPubUnroll; ++j) {
-    const int off = base + j * kPubThreads;
-    if (off >= upf) break;
-    const uint4 kin = ld_stream(src_k + off);
-    const uint4 vin = ld_stream(src_v + off);
-    uint4 qin = make_uint4(0, 0, 0, 0);
-    if (with_q) qin = ld_stream(q_in + off);
-    const int tok = div_small(off, p.units_per_row, p.inv_units_per_row);
-    const int in_row = off - tok * p.units_per_row;
-    const int pair0 = (in_row & (p.units_per_head - 1)) * 4;
-    const int ty = div_small(tok, p.frame_w, p.inv_frame_w);
-    const int tx = tok - ty * p.frame_w;
-    const uint32_t kw[4] = {kin.x, kin.y, kin.z, kin.w};
-    const uint32_t qw[4] = {qin.x, qin.y, qin.z, qin.w};
+  for (int j = 0; j < G; ++j) {
+    kin[j] = ld_stream(src_k + off0 + j * uph);
+    vin[j] = ld_stream(src_v + off0 + j * uph);
+    qin[j] = with_q ? ld_stream(q_in + off0 + j * uph) : make_uint4(0, 0, 0, 0);
+  }
+  const int ty = div_small(tok, p.frame_w, p.inv_frame_w);
+  const int tx = tok - ty * p.frame_w;
+  float2 cs[4];
+  const double* cs64[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int idx = rope_index(p, o * 4 + e, I.t, ty, tx);
+    cs[e] = __ldg(p.rope32 + idx);
+    cs64[e] = reinterpret_cast<const double*>(p.rope64 + idx);
+  }
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int off = off0 + j * uph;
+    const uint32_t kw[4] = {kin[j].x, kin[j].y, kin[j].z, kin[j].w};
+    const uint32_t qw[4] = {qin[j].x, qin[j].y, qin[j].z, qin[j].w};
     uint32_t ko[4], qo[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int idx = rope_index(p, pair0 + e, I.t, ty, tx);
-      const float2 cs = __ldg(p.rope32 + idx);
-      const double* cs64 = reinterpret_cast<const double*>(p.rope64 + idx);
-      ko[e] = rot_k_pair(kw[e], cs, cs64);
-      qo[e] = rot_q_pair(qw[e], cs);
+      ko[e] = rot_k_pair(kw[e], cs[e], cs64[e]);
+      qo[e] = rot_q_pair(qw[e], cs[e]);
     }
     st_u4(dst_k + off, make_uint4(ko[0], ko[1], ko[2], ko[3]));
-    st_u4(dst_v + off, vin);
+    st_u4(dst_v + off, vin[j]);
     if (with_q) st_u4(q_out + off, make_uint4(qo[0], qo[1], qo[2], qo[3]));
   }
 }
 
+namespace {
+template <int G, class P>
+void launch_publish_g(const P& p, int upf, int n_items, cudaStream_t s) {
+  dim3 grid((upf / G + kPubThreads - 1) / kPubThreads, n_items);
+  rope_publish_kernel<P::kItems, G><<<grid, kPubThreads, 0, s>>>(p);
+}
+template <class P>
+void launch_publish_p(const P& p, int upf, int heads, cudaStream_t s) {
+  if (heads % FF_PUB_G == 0)
+    launch_publish_g<FF_PUB_G>(p, upf, p.n_items, s);
+  else if (heads % 2 == 0)
+    launch_publish_g<2>(p, upf, p.n_items, s);
+  else
+    launch_publish_g<1>(p, upf, p.n_items, s);
+}
+}  // namespace
+
 cudaError_t launch_publish(const G1Params& p, int /*grid_hint*/, cudaStream_t s) {
   const int upf = static_cast<int>(p.units_per_frame);
-  dim3 grid((upf + kPubThreads * kPubUnroll - 1) / (kPubThreads * kPubUnroll), p.n_items);
+  const int heads = p.units_per_row / p.units_per_head;
   if (p.n_items <= kFewItems) {
     G1ParamsN<kFewItems> q{};
     static_cast<G1Header&>(q) = p;
     for (int i = 0; i < p.n_items; ++i) q.items[i] = p.items[i];
-    rope_publish_kernel<kFewItems><<<grid, kPubThreads, 0, s>>>(q);
+    launch_publish_p(q, upf, heads, s);
   } else {
-    rope_publish_kernel<kMaxItems><<<grid, kPubThreads, 0, s>>>(p);
+    launch_publish_p(p, upf, heads, s);
   }
   return cudaGetLastError();
 }
