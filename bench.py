@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # a kernel edited since then reports null.
 NCU_TRAFFIC = {
     "bank_attn_kernel": (221.1e6, "ff_attn.cu", "16db896386b0d636"),
-    "rope_publish_kernel": (45.4e6, "ff_publish.cu", "4fd14135b4e126b2"),
+    "rope_publish_kernel": (45.3e6, "ff_publish.cu", "a28235a92b5440a1"),
 }
 
 
