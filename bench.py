@@ -200,8 +200,7 @@ def run_gpu(args):
     T, H, D = 1560, 12, 128
     nq, nk, flops, g1_bytes = workload_numbers()
     steady_per_layer = 4 * (27 - 5)  # chunks 5..26 of each stage have full history
-    # warm-up, the timed region, then as many calls again with per-kernel events
-    total_calls = args.warmup + 2 * args.steps
+    total_calls = args.warmup + args.steps
     n_layers = max(1, math.ceil(total_calls / steady_per_layer))
     bank = ff.Bank(n_layers=n_layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
                    total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, device=local)
@@ -262,6 +261,7 @@ def run_gpu(args):
     for j in range(args.warmup):
         call(j)
     torch.cuda.synchronize()
+    bank.set_timing(True)
     sampler = ClockSampler(local, args.clock_ms)
     sampler.start()
     time.sleep(0.3)
@@ -274,8 +274,7 @@ def run_gpu(args):
     e0.record(stream)
     for ss in sstreams:
         ss.wait_event(e0)
-    timed_end = args.warmup + args.steps
-    for j in range(args.warmup, timed_end):
+    for j in range(args.warmup, total_calls):
         call(j)
     for ss in sstreams:
         done = torch.cuda.Event()
@@ -288,23 +287,6 @@ def run_gpu(args):
         pg.barrier()
     clocks = sampler.stop()
     ms_total = e0.elapsed_time(e1)
-    # per-kernel CUDA events (recorded by the library around each launch) slow the
-    # step a little, so they run in a second region of the same length right after
-    bank.set_timing(True)
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for ss in sstreams:
-        ss.wait_event(f0)
-    for j in range(timed_end, total_calls):
-        call(j)
-    for ss in sstreams:
-        done = torch.cuda.Event()
-        done.record(ss)
-        stream.wait_event(done)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    ms_instrumented = f0.elapsed_time(f1) / args.steps
     kt = bank.read_timing()
     bank.set_timing(False)
     assert bank.error_poll() == 0, "device-side wait timed out"
@@ -363,9 +345,7 @@ def run_gpu(args):
             "pct_bf16_peak": round(100 * value / peaks[bf16_key], 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
             "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
-                          "combine": round(comb_ms, 4),
-                          "source": f"CUDA events around each launch, in a second region of {args.steps} steps "
-                                    f"right after the timed one ({ms_instrumented:.4f} ms per step with the events)"},
+                          "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
             "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
