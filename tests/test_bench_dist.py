@@ -84,3 +84,21 @@ def test_clock_summary_keeps_samples_inside_the_timed_window():
     c.mark(now + 10.0, now + 11.0)
     r = c.stop()
     assert r["samples"] == 4 and r["window"].startswith("all samples")
+
+
+def test_peaks_from_measured_file_or_fallback(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, src = bench.load_peaks()
+    assert src == "fallback" and peaks == bench.FALLBACK_PEAKS
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": {"value": 7100.0}, "bf16_tflops": 2010.5, "bf16_tflops_sustained": {"value": 1790.0},
+         "clocks": {"sm_mhz": 2070}}))
+    peaks, src = bench.load_peaks()
+    assert src == "measured"
+    assert peaks == {"hbm_gbs": 7100.0, "bf16_tflops": 2010.5, "bf16_tflops_sustained": 1790.0}
+    (tmp_path / "MEASURED_PEAKS.json").write_text("{not json")
+    assert bench.load_peaks()[1] == "fallback"
