@@ -479,6 +479,7 @@ class OracleBank:
             vs.append(sl.v)
         for j in history_chunks(chunk, c.history):
             sl = self.stage[layer][stage][bank_slot(j, c.history)]
+            assert sl.tag == j, "Tail_H invariant broken"
             ks.append(sl.k)
             vs.append(sl.v)
         pos = token_positions(own, c.frame_h, c.frame_w)
