@@ -75,6 +75,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# nominal dense bf16 tensor rate of one GB300 (HGX B300 datasheet: 36 PFLOP/s with
+# 2:4 sparsity per 8 GPUs = 2.25 PFLOP/s dense per GPU); context beside the measured peaks
+DATASHEET_BF16_TFLOPS = 2250.0
+
+
+def bench_config(world=1, stage_streams=1):
+    """The `config` of the JSON line: the same dict for the GPU arm and the
+    reference (oracle) arm."""
+    return {"workload": WORKLOAD, "heads": 12, "head_dim": 128, "tokens_per_frame": 1560, "queries": 4680,
+            "keys": 31200, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
+            "parallelism": "replicas" if world > 1 else "single GPU", "stage_streams": stage_streams,
+            "l2": "inputs larger than L2 (~300 MB touched per call)"}
+
+
 def workload_numbers(T=1560, heads=12, d=128, nq_frames=3, key_frames=20):
     nq, nk = nq_frames * T, key_frames * T
     flops = 4.0 * nq * nk * d * heads
@@ -306,11 +320,22 @@ def run_gpu(args):
     pub_gbs = g1_bytes / (pub_ms * 1e-3) / 1e9
     roofline = {"kernel": "bank_attn_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
                 "peak": peaks[bf16_key], "unit": "TFLOP/s", "frac": round(attn_tflops / peaks[bf16_key], 4),
-                "traffic": ncu_traffic("bank_attn_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} {bf16_key} ({bf16_label})",
+                "traffic": ncu_traffic("bank_attn_kernel"), "traffic_unit": "bytes/launch",
+                "peak_source": f"{peak_src} {bf16_key} ({bf16_label})",
+                # the same launch against every denominator, side by side
+                "frac_of_burst": round(attn_tflops / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": (round(attn_tflops / peaks["bf16_tflops_sustained"], 4)
+                                      if "bf16_tflops_sustained" in peaks else None),
+                "frac_of_datasheet": round(attn_tflops / DATASHEET_BF16_TFLOPS, 4),
+                "datasheet_peak": DATASHEET_BF16_TFLOPS,
                 "algorithmic_per_launch": f"{flops / 1e9:.1f} GFLOP (4*Nq*Nk*d*h)", "avg_launch_ms": round(attn_ms, 4)}
+    pub_traffic = ncu_traffic("rope_publish_kernel")
     roofline_publish = {"kernel": "rope_publish_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
-                        "traffic": ncu_traffic("rope_publish_kernel"), "traffic_unit": "bytes/launch", "peak_source": f"{peak_src} hbm_gbs",
+                        "achieved_is": "effective bandwidth: algorithmic bytes / launch time (its writes stay in L2)",
+                        "traffic": pub_traffic, "traffic_unit": "bytes/launch",
+                        "dram_gbs": round(pub_traffic / (pub_ms * 1e-3) / 1e9, 1) if pub_traffic else None,
+                        "peak_source": f"{peak_src} hbm_gbs",
                         "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (18 frames x 4.79 MB)",
                         "avg_launch_ms": round(pub_ms, 4)}
 
@@ -337,12 +362,9 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded AR(1) unit-RMS Q/K, N(0,1) V)",
-            "config": {"workload": WORKLOAD, "heads": H, "head_dim": D, "tokens_per_frame": T, "queries": nq,
-                       "keys": nk, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "stage_streams": n_streams,
-                       "l2": "inputs larger than L2 (~300 MB touched per call)"},
+            "config": bench_config(world, n_streams),
             "pct_bf16_peak": round(100 * value / peaks[bf16_key], 2),
+            "pct_bf16_datasheet": round(100 * value / DATASHEET_BF16_TFLOPS, 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
             "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
@@ -757,31 +779,35 @@ def oracle_tiny_bruteforce():
 
 
 def run_reference(args):
+    """The oracle arm: fp64 numpy attention of the steady 1.3B call on the host
+    cores.  Every step is a bounded sample of that call (all 12 heads, the
+    first R query rows over all 31200 keys), R sized so that the warm-up and
+    timed steps take about three minutes together."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    dt0, f0 = oracle_sample(64, 1)
+    dt0, f0 = oracle_sample(64, 12)
     rate = f0 / max(dt0, 1e-6)
-    # each step: a bounded sample sized so that all steps take about a minute
-    per_step_s = max(0.05, 60.0 / max(args.steps + args.warmup, 1))
-    rows = int(min(4680, max(16, per_step_s * rate / (4.0 * 31200 * 128))))
+    per_step_s = max(0.05, 180.0 / max(args.steps + args.warmup, 1))
+    per_row = 4.0 * 31200 * 128 * 12
+    rows = int(min(4680, max(16, per_step_s * rate / per_row)))
     times, fl = [], 0.0
     for j in range(args.warmup + args.steps):
-        dt, fl = oracle_sample(rows, 1, seed=j)
+        dt, fl = oracle_sample(rows, 12, seed=j)
         if j >= args.warmup:
             times.append(dt)
     total = sum(times)
     value = fl * len(times) / total / 1e12
     cores = _host_cores()
-    sample = (f"fp64 numpy oracle attention, {rows} query rows x 1 head x 31200 keys per step "
-              f"({fl / 1e9:.2f} GFLOP/step) of the steady 1.3B call")
+    sample = (f"fp64 numpy oracle attention per step: {rows} of the 4680 query rows x 12 heads x 31200 keys "
+              f"({fl / 1e9:.2f} GFLOP/step) of the steady 1.3B call; rope/publish not included")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / len(times), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "heads": 12, "head_dim": 128, "queries": 4680, "keys": 31200},
+        "config": bench_config(world, max(1, min(4, args.stage_streams))),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "blas_threads": _blas_threads()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -15,8 +15,10 @@
  *
  * This library implements the attention part of F_R for one transformer
  * layer per call: rotary position encoding of the chunk's Q/K, publish of
- * (K, V) into the stage bank, gather of anchors + history + own K/V into a
- * contiguous context, and softmax(Q K^T / sqrt(d)) V over that context.
+ * (K, V) into the stage bank, and softmax(Q K^T / sqrt(d)) V over the context
+ * [anchors of Gamma(i); last H chunks of the stage; own chunk].  The context
+ * is never copied into one buffer: the attention kernel's TMA tensor loads
+ * read the anchor slots and the stage-ring slots where they live.
  *
  * Conventions for every entry point:
  *  - Tensors are bf16, row-major [tokens, heads, head_dim] with tokens
@@ -30,7 +32,13 @@
  *    memory it allocates.  No call allocates device memory after
  *    ff_bank_create.
  *  - Every call returns an ff_status.  On any error the bank state is left
- *    unchanged and nothing is enqueued.  Nothing aborts the process.
+ *    unchanged.  Argument, order and residency errors are found before any
+ *    work is enqueued.  FF_ERR_CUDA from a kernel launch that fails after an
+ *    earlier kernel of the same call was enqueued (ff_render_attn: the
+ *    publish kernel runs before the attention kernel) leaves that earlier
+ *    work enqueued; it wrote only memory that no resident chunk occupies, so
+ *    the observable bank state is still unchanged.  Nothing aborts the
+ *    process.
  *  - A bank may be used from one host thread at a time.
  */
 #ifndef FF_H_
@@ -82,9 +90,11 @@ typedef struct ff_bank ff_bank_t;
  * 30 x 52 tokens, 9 anchor slots, device 0). */
 int ff_desc_default(ff_bank_desc* d);
 
-/* Allocate every device buffer the bank will ever use: the S x H stage
- * slots and the anchor ring of every layer, per-stage context and Q
- * scratch, the attention split scratch and the rotary tables.  Returns
+/* Allocate every device buffer the bank will ever use: the stage rings
+ * (H + 1 physical chunk slots per (layer, stage), so that chunk i can be
+ * written while chunks i-H .. i-1 are read in place) and the anchor ring of
+ * every layer, per-stage rotated-Q scratch and attention split partials, the
+ * planner scratch and the rotary tables.  Returns
  * FF_ERR_ARG for an invalid description, FF_ERR_UNSUPPORTED if the device
  * is not sm_103, FF_ERR_OOM if the total exceeds max_bytes or an allocation
  * fails (nothing stays allocated then).  *out is set only on FF_OK. */
@@ -245,20 +255,25 @@ int ff_bank_wait_probe(ff_bank_t* bank, int limit_ms, void* stream);
  * out = softmax(q k^T / sqrt(head_dim)) v per head, computed by the same
  * tcgen05 kernel as ff_render_attn.  q, out: device bf16 [nq, heads, head_dim];
  * k, v: device bf16 [nk, heads, head_dim]; all 16-byte aligned, owned by the
- * caller; head_dim 64 or 128.  Asynchronous on `stream` (a cudaStream_t).
+ * caller, on the current device; head_dim 64 or 128.  Asynchronous on `stream`
+ * (a cudaStream_t of the current device).
  *
  * Scratch: key-range split partials live in one static device array of
  * FF_NOALLOC_SCRATCH_BYTES, created when the library's module loads on a
- * device and kept until the process exits.  A call needs
- * 256 + heads * ceil(nq/256) * n_split * 256 * (4 * head_dim + 8) bytes of it
- * (n_split in 2..4 chosen by the library, 1 when nk <= 128); larger problems
- * are rejected with FF_ERR_ARG before any work is enqueued.  The first call
- * on a device (that device current) sets up the array's address and the
- * kernel attributes: make it before any stream capture.  All calls share the
- * array, so calls that overlap on the GPU race; order them on one stream.
- * A bounded device wait that gives up leaves `out` undefined and is not
- * reported by this entry point.  Returns FF_OK, FF_ERR_ARG, FF_ERR_CUDA or
- * FF_ERR_UNSUPPORTED (device not sm_103). */
+ * device and kept until the process exits.  The work plan is the bank path's
+ * (whole units first, the rest cut into up to 4 key ranges), restricted to
+ * plans whose partials fit: a split plan needs
+ * 256 + split_units * n_split * 256 * (4 * head_dim + 8) bytes, and the plan
+ * without a split needs none, so no problem is refused for its size.  Sizes
+ * beyond the kernels' index limits (more than 2^24 key tiles of 128 or
+ * (head, 256-row query block) units, or 2^31 elements per tensor) are refused
+ * with FF_ERR_ARG before any work is enqueued.  The first call on a device
+ * (that device current) sets up the array's address and the kernel
+ * attributes: make it before any stream capture.  All calls share the array,
+ * so calls that overlap on the GPU race; order them on one stream.  A bounded
+ * device wait that gives up leaves `out` undefined and is not reported by
+ * this entry point.  Returns FF_OK, FF_ERR_ARG (also for a stream of another
+ * device), FF_ERR_CUDA or FF_ERR_UNSUPPORTED (device not sm_103). */
 #define FF_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 int ff_attention_noalloc(const void* q, const void* k, const void* v, void* out, int nq, int nk, int heads,
                          int head_dim, void* stream);

@@ -123,9 +123,11 @@ struct ff_bank {
   cudaStream_t planner_stream = nullptr;
   bool planner_used = false;
 
-  // timing
+  // timing: a pool of event sets created by ff_bank_set_timing, reused by
+  // later calls (the first n_timed are in use since the last reset)
   bool timing = false;
   std::vector<TimedCall> timed;
+  size_t n_timed = 0;
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 
@@ -215,52 +217,6 @@ void plan_planner(const ff_bank_desc& d, int b, ff_planner_plan* p) {
   p->n_hist_blocks = b - p->hist_first_block;
   p->hist_frames = p->n_hist_blocks * d.planner_block;
   p->key_frames = p->hist_frames + p->n_anchors;
-}
-
-// Work plan of an attention call with `units` (head, query block) units of
-// n_kv key tiles on `sms` persistent CTAs: the first n_whole units run as one
-// piece each, the others as n_split key ranges merged by the combine kernel.
-// Candidates are whole waves of whole units followed by split units; each is
-// scored by the round-robin makespan in tiles (+2 per piece for its prologue
-// and epilogue) plus the combine's cost (about 1e-4 tile per partial row).
-struct SplitPlan {
-  int n_whole, n_split, n_pieces;
-  size_t part_rows;
-};
-
-SplitPlan plan_split(int units, int n_kv, int sms, size_t max_part_rows) {
-  SplitPlan best{units, 1, units, 0};
-  double best_cost = 1e300;
-  std::vector<double> load(static_cast<size_t>(std::max(sms, 1)));
-  for (int ns = 1; ns <= std::min(kMaxSplit, n_kv); ++ns) {
-    for (int m = 0; m * sms <= units; ++m) {
-      const int n_whole = (ns == 1) ? units : m * sms;
-      const int rest = units - n_whole;
-      if (ns > 1 && rest == 0) continue;
-      const size_t rows = static_cast<size_t>(rest) * ns * 256;
-      if (ns > 1 && rows > max_part_rows) continue;
-      const int pieces = n_whole + rest * ns;
-      const int grid = std::min(pieces, sms);
-      std::fill(load.begin(), load.begin() + grid, 0.0);
-      for (int pc = 0; pc < pieces; ++pc) {
-        int tiles = n_kv;
-        if (pc >= n_whole) {
-          const int split = (pc - n_whole) / rest;
-          tiles = static_cast<int>((static_cast<long long>(split + 1) * n_kv) / ns -
-                                   (static_cast<long long>(split) * n_kv) / ns);
-        }
-        load[pc % grid] += tiles + 2.0;
-      }
-      double cost = *std::max_element(load.begin(), load.begin() + grid);
-      if (ns > 1) cost += 4.0 + static_cast<double>(rows) * 1e-4;
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        best = {n_whole, ns, pieces, ns > 1 ? rows : 0};
-      }
-      if (ns == 1) break;
-    }
-  }
-  return best;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -367,28 +323,34 @@ int build_segments(const ff_bank* b, const std::vector<SegSpec>& seg, Base base,
   return FF_OK;
 }
 
-// Launch attention (and the split combine) for the query groups in `ap`
-// (heads, out, err, scale and groups filled by the caller) over the K/V maps
-// `kv`.  Partial rows beyond `part_rows` disable splitting.  With `tc`, ev[2]
-// is recorded between attention and combine.
-int attend(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, const KVMaps& kv, float* part_o,
-           float* part_ml, size_t part_rows, bool allow_split, cudaStream_t s, TimedCall* tc) {
-  const ff_bank_desc& d = b->d;
+// Work plan and Q tensor map of an attention launch for the query groups in
+// `ap` (heads, out, err, scale and groups filled by the caller): everything
+// that can fail before a kernel is enqueued.  Partial rows beyond `part_rows`
+// disable splitting.
+int prepare_attention(const ff_bank* b, AttnParams& ap, const void* q, int q_rows, float* part_o, float* part_ml,
+                      size_t part_rows, bool allow_split, CUtensorMap* tq) {
   ap.part_o = part_o;
   ap.part_ml = part_ml;
-  int rc;
-  CUtensorMap tq;
-  if ((rc = make_map(b, &tq, q, q_rows)) != FF_OK) return rc;
-  const int units = d.heads * ap.n_qb;
+  const int rc = make_map(b, tq, q, q_rows);
+  if (rc != FF_OK) return rc;
+  const int units = b->d.heads * ap.n_qb;
   SplitPlan sp{units, 1, units, 0};
   if (ap.n_groups == 1 && allow_split) sp = plan_split(units, ap.groups[0].n_kv, b->sm_count, part_rows);
   ap.n_whole = sp.n_whole;
   ap.n_split = sp.n_split;
   ap.n_pieces = sp.n_pieces;
+  return FF_OK;
+}
+
+// Launch attention (and the split combine) prepared by prepare_attention over
+// the K/V maps `kv`.  With `tc`, ev[2] is recorded between attention and combine.
+int attend(const ff_bank* b, const AttnParams& ap, const CUtensorMap& tq, const KVMaps& kv, cudaStream_t s,
+           TimedCall* tc) {
+  int rc;
   const int grid = std::min(ap.n_pieces, b->sm_count);
-  if ((rc = cuda_err(launch_attention(d.head_dim, tq, kv, ap, grid, s), "attention launch")) != FF_OK) return rc;
+  if ((rc = cuda_err(launch_attention(b->d.head_dim, tq, kv, ap, grid, s), "attention launch")) != FF_OK) return rc;
   if (tc) cudaEventRecord(tc->ev[2], s);
-  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
+  if (ap.n_split > 1 && (rc = cuda_err(launch_combine(b->d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
   if (tc) tc->combine = ap.n_split > 1;
   return FF_OK;
 }
@@ -409,6 +371,8 @@ G1Params publish_params(const ff_bank* b) {
   prm.pt = b->pt;
   prm.py = b->py;
   prm.px = b->px;
+  prm.err = b->err;
+  prm.sm_count = b->sm_count;
   return prm;
 }
 
@@ -454,6 +418,35 @@ int alloc(ff_bank* b, size_t bytes, void** out) {
   }
   b->allocations.push_back(p);
   *out = p;
+  return FF_OK;
+}
+
+// Timing event sets: kTimedPool are created when timing is switched on, so a
+// timed render records into existing events; a run with more calls between
+// resets grows the pool by that many again.
+constexpr size_t kTimedPool = 2048;
+
+int grow_timed(ff_bank* b, size_t n) {
+  for (size_t j = 0; j < n; ++j) {
+    TimedCall tc{};
+    for (auto& e : tc.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) {
+        for (auto& f : tc.ev)
+          if (f) cudaEventDestroy(f);
+        return FF_ERR_CUDA;
+      }
+    b->timed.push_back(tc);
+  }
+  return FF_OK;
+}
+
+int next_timed_call(ff_bank* b, TimedCall** tc) {
+  if (b->n_timed == b->timed.size()) {
+    const int rc = grow_timed(b, kTimedPool);
+    if (rc != FF_OK) return rc;
+  }
+  *tc = &b->timed[b->n_timed];
+  (*tc)->combine = false;
   return FF_OK;
 }
 
@@ -860,20 +853,21 @@ int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_
   for (int j = 0; j < pl.n_anchors; ++j)
     if (b->anchor_used[aslots[j]] && b->anchor_stream[aslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[aslots[j]], 0);
 
-  TimedCall tc{};
+  CUtensorMap tq;
+  if ((rc = prepare_attention(b, ap, sc.q_rot, nq, sc.part_o, sc.part_ml, b->part_rows, true, &tq)) != FF_OK) return rc;
+  TimedCall* tc = nullptr;
   if (b->timing) {
-    for (auto& e : tc.ev)
-      if (cudaEventCreate(&e) != cudaSuccess) return FF_ERR_CUDA;
-    cudaEventRecord(tc.ev[0], s);
+    if ((rc = next_timed_call(b, &tc)) != FF_OK) return rc;
+    cudaEventRecord(tc->ev[0], s);
   }
+
+  // ---- nothing below fails for a reason that can be checked beforehand
   if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
-  if (b->timing) cudaEventRecord(tc.ev[1], s);
-  if ((rc = attend(b, ap, sc.q_rot, nq, kv, sc.part_o, sc.part_ml, b->part_rows, true, s, b->timing ? &tc : nullptr)) !=
-      FF_OK)
-    return rc;
-  if (b->timing) {
-    cudaEventRecord(tc.ev[3], s);
-    b->timed.push_back(tc);
+  if (tc) cudaEventRecord(tc->ev[1], s);
+  if ((rc = attend(b, ap, tq, kv, s, tc)) != FF_OK) return rc;
+  if (tc) {
+    cudaEventRecord(tc->ev[3], s);
+    ++b->n_timed;
   }
   cudaEventRecord(b->ev_stage[stage], s);
   b->stage_stream[stage] = s;
@@ -939,12 +933,14 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
                           ap.groups[0], kv);
   if (rc != FF_OK) return rc;
 
+  CUtensorMap tq;
+  if ((rc = prepare_attention(b, ap, sc.q_rot, nq, sc.part_o, sc.part_ml, b->planner_part_rows, true, &tq)) != FF_OK)
+    return rc;
   if (b->planner_used && b->planner_stream != s) cudaStreamWaitEvent(s, b->ev_planner, 0);
   for (int j = 0; j < n_hist; ++j)
     if (b->anchor_used[hslots[j]] && b->anchor_stream[hslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[hslots[j]], 0);
   if ((rc = cuda_err(launch_publish(prm, 0, s), "planner rope launch")) != FF_OK) return rc;
-  if ((rc = attend(b, ap, sc.q_rot, nq, kv, sc.part_o, sc.part_ml, b->planner_part_rows, true, s, nullptr)) != FF_OK)
-    return rc;
+  if ((rc = attend(b, ap, tq, kv, s, nullptr)) != FF_OK) return rc;
   cudaEventRecord(b->ev_planner, s);
   b->planner_stream = s;
   b->planner_used = true;
@@ -1045,7 +1041,9 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       kv.k[m] = kv.k[0];
       kv.v[m] = kv.v[0];
     }
-    if ((rc = attend(b, ap, qrot, static_cast<int>(N * T), kv, nullptr, nullptr, 0, false, s, nullptr)) != FF_OK)
+    CUtensorMap tq;
+    if ((rc = prepare_attention(b, ap, qrot, static_cast<int>(N * T), nullptr, nullptr, 0, false, &tq)) != FF_OK ||
+        (rc = attend(b, ap, tq, kv, s, nullptr)) != FF_OK)
       return rc;
   }
   return FF_OK;
@@ -1075,17 +1073,17 @@ int ff_bank_set_timing(ff_bank_t* b, int enable) {
   if (!b) return FF_ERR_ARG;
   cudaSetDevice(b->d.device);
   cudaDeviceSynchronize();
-  for (auto& tc : b->timed)
-    for (cudaEvent_t e : tc.ev) cudaEventDestroy(e);
-  b->timed.clear();
+  b->n_timed = 0;
   b->timing = enable != 0;
+  if (b->timing && b->timed.empty()) return grow_timed(b, kTimedPool);
   return FF_OK;
 }
 
 int ff_bank_read_timing(ff_bank_t* b, ff_kernel_times* out) {
   if (!b || !out) return FF_ERR_ARG;
   std::memset(out, 0, sizeof(*out));
-  for (auto& tc : b->timed) {
+  for (size_t j = 0; j < b->n_timed; ++j) {
+    const TimedCall& tc = b->timed[j];
     if (cudaEventSynchronize(tc.ev[3]) != cudaSuccess) return FF_ERR_CUDA;
     float a = 0, c = 0, e = 0;
     cudaEventElapsedTime(&a, tc.ev[0], tc.ev[1]);

@@ -1,8 +1,10 @@
 // Structures shared by the host side of libff (ff_bank.cpp) and its kernels.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,6 +47,8 @@ struct G1Header {
   int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
   int px;
   int n_items;
+  unsigned int* err;          // device error word (bounded waits of the staged kernel)
+  int sm_count;               // SMs of the device (persistent grid of the staged kernel)
 };
 
 template <int N>
@@ -129,6 +133,54 @@ inline void attn_single_group(AttnParams& p, int nq, int nk) {
   g.seg_tile0[0] = 0;
   g.n_kv = (nk + 127) / 128;
   p.n_qb = (nq + 255) / 256;
+}
+
+// Work plan of an attention call with `units` (head, query block) units of
+// n_kv key tiles on `sms` persistent CTAs: the first n_whole units run as one
+// piece each, the others as n_split key ranges merged by the combine kernel.
+// Candidates are whole waves of whole units followed by split units (and the
+// plan with no split at all, which needs no partials); each is scored by the
+// round-robin makespan in tiles (+2 per piece for its prologue and epilogue)
+// plus the combine's cost (about 1e-4 tile per partial row).  Split plans
+// whose partials exceed max_part_rows rows are not considered.
+struct SplitPlan {
+  int n_whole, n_split, n_pieces;
+  size_t part_rows;
+};
+
+inline SplitPlan plan_split(int units, int n_kv, int sms, size_t max_part_rows) {
+  SplitPlan best{units, 1, units, 0};
+  double best_cost = 1e300;
+  std::vector<double> load(static_cast<size_t>(std::max(sms, 1)));
+  for (int ns = 1; ns <= std::min(kMaxSplit, n_kv); ++ns) {
+    for (int m = 0; m * sms <= units; ++m) {
+      const int n_whole = (ns == 1) ? units : m * sms;
+      const int rest = units - n_whole;
+      if (ns > 1 && rest == 0) continue;
+      const size_t rows = static_cast<size_t>(rest) * ns * 256;
+      if (ns > 1 && rows > max_part_rows) continue;
+      const int pieces = n_whole + rest * ns;
+      const int grid = std::min(pieces, sms);
+      std::fill(load.begin(), load.begin() + grid, 0.0);
+      for (int pc = 0; pc < pieces; ++pc) {
+        int tiles = n_kv;
+        if (pc >= n_whole) {
+          const int split = (pc - n_whole) / rest;
+          tiles = static_cast<int>((static_cast<long long>(split + 1) * n_kv) / ns -
+                                   (static_cast<long long>(split) * n_kv) / ns);
+        }
+        load[pc % grid] += tiles + 2.0;
+      }
+      double cost = *std::max_element(load.begin(), load.begin() + grid);
+      if (ns > 1) cost += 4.0 + static_cast<double>(rows) * 1e-4;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = {n_whole, ns, pieces, ns > 1 ? rows : 0};
+      }
+      if (ns == 1) break;
+    }
+  }
+  return best;
 }
 
 // Host launchers (ff_publish.cu / ff_attn.cu).

@@ -17,6 +17,12 @@
 // the attention kernel's shared-memory attribute.  Make that first call before
 // any stream capture.  Later calls only enqueue work.
 //
+// Work plan: the same planner as the bank path (whole waves of whole units,
+// then at most kMaxSplit key ranges for the rest), limited to plans whose
+// partials fit the array.  The plan without any split needs no partials, so
+// every problem within the kernels' index limits runs; a large problem (many
+// heads, long query runs) simply runs whole units only.
+//
 // Sharing: every call on a device uses the same array and leaves its contents
 // there.  Split partials are fully rewritten by each call before they are read;
 // the kernel's error word (the array's first bytes) is cleared on the call's
@@ -42,23 +48,6 @@ std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-// Same cost model as the bank path, restricted to real splits (s >= 2).
-int split_for(int units, int n_kv, int sms) {
-  if (n_kv < 2) return 1;
-  double best = 1e300;
-  int best_s = 2;
-  for (int s = 2; s <= (n_kv < ff::kMaxSplit ? n_kv : ff::kMaxSplit); ++s) {
-    const long long pieces = static_cast<long long>(units) * s;
-    const long long waves = (pieces + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (static_cast<double>(n_kv) / s + 2.0);
-    if (cost < best - 1e-9) {
-      best = cost;
-      best_s = s;
-    }
-  }
-  return best_s;
-}
 
 int setup(int dev, void** scratch, int* sms) {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -114,9 +103,21 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
     if (reinterpret_cast<uintptr_t>(p) & 15u) return FF_ERR_ARG;
   const int n_qb = (nq + 255) / 256;
   const long long n_kv = (static_cast<long long>(nk) + 127) / 128;
-  if (n_kv > (1 << 24) || static_cast<long long>(heads) * n_qb > (1 << 24)) return FF_ERR_ARG;
+  // index limits of the kernels: key tiles and (head, query block) units are ints,
+  // row offsets (row * heads * head_dim) stay below 2^31 elements per tensor
+  if (n_kv > (1 << 24) || static_cast<long long>(heads) * n_qb > (1 << 24) ||
+      static_cast<long long>(nq) * heads * head_dim >= (1ll << 31) ||
+      static_cast<long long>(nk) * heads * head_dim >= (1ll << 31))
+    return FF_ERR_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FF_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int sdev = -1;
+  if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+    cudaGetLastError();
+    return FF_ERR_ARG;
+  }
+  if (sdev != dev) return FF_ERR_ARG;  // the stream belongs to another device than the current one
   void* scratch = nullptr;
   int sms = 0;
   const int rc = setup(dev, &scratch, &sms);
@@ -126,12 +127,12 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
   ap.out = out;
   ap.heads = heads;
   ff::attn_single_group(ap, nq, nk);
-  ap.n_split = split_for(heads * n_qb, ap.groups[0].n_kv, sms);
-  ap.n_whole = ap.n_split > 1 ? 0 : heads * n_qb;  // every unit split, or none
-  ap.n_pieces = heads * n_qb * ap.n_split;
-  const size_t part_rows = static_cast<size_t>(ap.n_pieces) * 256;
-  const size_t need = kErrBytes + part_rows * static_cast<size_t>(head_dim) * 4 + part_rows * 8;
-  if (ap.n_split > 1 && need > FF_NOALLOC_SCRATCH_BYTES) return FF_ERR_ARG;  // beyond the static scratch
+  const size_t max_part_rows = (FF_NOALLOC_SCRATCH_BYTES - kErrBytes) / (static_cast<size_t>(head_dim) * 4 + 8);
+  const ff::SplitPlan sp = ff::plan_split(heads * n_qb, ap.groups[0].n_kv, sms, max_part_rows);
+  ap.n_whole = sp.n_whole;
+  ap.n_split = sp.n_split;
+  ap.n_pieces = sp.n_pieces;
+  const size_t part_rows = sp.part_rows;  // 0 without a split
   unsigned char* base = static_cast<unsigned char*>(scratch);
   ap.err = reinterpret_cast<unsigned int*>(base);
   ap.part_o = reinterpret_cast<float*>(base + kErrBytes);
@@ -147,7 +148,6 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
     kv.k[m] = kv.k[0];
     kv.v[m] = kv.v[0];
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ap.err, 0, sizeof(unsigned int), s) != cudaSuccess) return FF_ERR_CUDA;
   const int grid = ap.n_pieces < sms ? ap.n_pieces : sms;
   if (ff::launch_attention(head_dim, tq, kv, ap, grid, s) != cudaSuccess) return FF_ERR_CUDA;

@@ -140,12 +140,19 @@ def plan_planner_block(desc: BankDesc, block: int) -> PlannerPlan:
 
 def attention_noalloc(q, k, v, out, stream=None):
     """Attention over a caller-held context without any device allocation
-    (see ff_attention_noalloc in include/ff.h)."""
+    (see ff_attention_noalloc in include/ff.h).  All four tensors must be on
+    one device; the call runs with that device current."""
+    import torch
     nq, heads, d = q.shape
     nk = k.shape[0]
-    _check(_lib().ff_attention_noalloc(_ptr(q, (nq, heads, d), "q"), _ptr(k, (nk, heads, d), "k"),
-                                       _ptr(v, (nk, heads, d), "v"), _ptr(out, (nq, heads, d), "out"),
-                                       nq, nk, heads, d, _stream(stream, q.device)), "ff_attention_noalloc")
+    if any(t.device != q.device for t in (k, v, out)):
+        raise ValueError("q, k, v and out must be on one device")
+    if stream is not None and stream.device != q.device:
+        raise ValueError("stream belongs to another device than the tensors")
+    with torch.cuda.device(q.device):
+        _check(_lib().ff_attention_noalloc(_ptr(q, (nq, heads, d), "q"), _ptr(k, (nk, heads, d), "k"),
+                                           _ptr(v, (nk, heads, d), "v"), _ptr(out, (nq, heads, d), "out"),
+                                           nq, nk, heads, d, _stream(stream, q.device)), "ff_attention_noalloc")
 
 
 class _DevView:
