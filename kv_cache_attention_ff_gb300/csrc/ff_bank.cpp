@@ -371,8 +371,6 @@ G1Params publish_params(const ff_bank* b) {
   prm.pt = b->pt;
   prm.py = b->py;
   prm.px = b->px;
-  prm.err = b->err;
-  prm.sm_count = b->sm_count;
   return prm;
 }
 

@@ -47,8 +47,6 @@ struct G1Header {
   int pt, py;                 // channel pairs on the time and row axes (pairs beyond pt+py: column axis)
   int px;
   int n_items;
-  unsigned int* err;          // device error word (bounded waits of the staged kernel)
-  int sm_count;               // SMs of the device (persistent grid of the staged kernel)
 };
 
 template <int N>
