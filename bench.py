@@ -80,12 +80,13 @@ def load_peaks():
 DATASHEET_BF16_TFLOPS = 2250.0
 
 
-def bench_config(world=1, stage_streams=1):
+def bench_config(world=1, stage_streams=1, batch=1):
     """The `config` of the JSON line: the same dict for the GPU arm and the
     reference (oracle) arm."""
     return {"workload": WORKLOAD, "heads": 12, "head_dim": 128, "tokens_per_frame": 1560, "queries": 4680,
             "keys": 31200, "anchors": 2, "history_chunks": 5, "chunk_frames": 3, "stages": 4,
             "parallelism": "replicas" if world > 1 else "single GPU", "stage_streams": stage_streams,
+            "calls_per_launch": batch,
             "l2": "inputs larger than L2 (~300 MB touched per call)"}
 
 
@@ -255,7 +256,6 @@ def run_gpu(args):
                 seq.append((key[0], key[1], next_chunk[key]))
                 next_chunk[key] += 1
     assert all(c >= 5 for _, _, c in seq)
-    kernels_per_call = bank.kernel_count(10)
 
     # one CUDA stream per denoising stage: calls of different stages are independent
     # (anti-diagonal chunks of the stage wavefront), so one stage's HBM-bound
@@ -272,8 +272,26 @@ def run_gpu(args):
         if rc != 0:
             raise RuntimeError(f"ff_render_attn failed with status {rc}")
 
-    for j in range(args.warmup):
-        call(j)
+    def call_batch(j0, j1):
+        # consecutive calls rotate over the 4 stages: every batch has distinct stages
+        calls = []
+        for j in range(j0, j1):
+            layer, st, c = seq[j]
+            q, k, v = pool[st][j % 4]
+            calls.append((layer, st, c, q.data_ptr(), k.data_ptr(), v.data_ptr(), souts[st].data_ptr()))
+        rc = bank.render_attn_batch_raw(calls, stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"ff_render_attn_batch failed with status {rc}")
+
+    def run_calls(j0, j1):
+        if args.batch <= 1:
+            for j in range(j0, j1):
+                call(j)
+        else:
+            for jb in range(j0, j1, args.batch):
+                call_batch(jb, min(j1, jb + args.batch))
+
+    run_calls(0, args.warmup)
     torch.cuda.synchronize()
     bank.set_timing(True)
     sampler = ClockSampler(local, args.clock_ms)
@@ -288,8 +306,7 @@ def run_gpu(args):
     e0.record(stream)
     for ss in sstreams:
         ss.wait_event(e0)
-    for j in range(args.warmup, total_calls):
-        call(j)
+    run_calls(args.warmup, total_calls)
     for ss in sstreams:
         done = torch.cuda.Event()
         done.record(ss)
@@ -362,14 +379,14 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded AR(1) unit-RMS Q/K, N(0,1) V)",
-            "config": bench_config(world, n_streams),
+            "config": bench_config(world, n_streams, args.batch),
             "pct_bf16_peak": round(100 * value / peaks[bf16_key], 2),
             "pct_bf16_datasheet": round(100 * value / DATASHEET_BF16_TFLOPS, 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
             "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kernels_per_call * args.steps, "clocks": clocks,
+            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kt.launches, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -805,7 +822,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / len(times), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": bench_config(world, max(1, min(4, args.stage_streams))),
+        "config": bench_config(world, max(1, min(4, args.stage_streams)), args.batch),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample, "blas_threads": _blas_threads()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -824,9 +841,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass (profiling runs)")
     ap.add_argument("--stage-streams", type=int, default=1,
                     help="CUDA streams the 4 stages are issued on (1..4); per-kernel event times need 1")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="calls per ff_render_attn_batch (1 = one ff_render_attn per step; 2..4 = stage wavefront "
+                         "batches of consecutive calls, which have distinct stages)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not 1 <= args.batch <= 4 or (args.batch > 1 and args.stage_streams > 1):
+        ap.error("--batch must be 1..4 (and with one stream)")
     if args.impl == "reference":
         run_reference(args)
     else:

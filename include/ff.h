@@ -124,6 +124,32 @@ int ff_anchor_publish(ff_bank_t* bank, int layer, int first_anchor_frame, int n_
 int ff_render_attn(ff_bank_t* bank, int layer, int stage, int chunk,
                    const void* q_pre, const void* k_pre, const void* v, void* out, void* stream);
 
+/* One renderer call of a batch: the arguments of ff_render_attn. */
+typedef struct ff_render_call {
+  int layer;
+  int stage;
+  int chunk;
+  const void* q_pre;
+  const void* k_pre;
+  const void* v;
+  void* out;
+} ff_render_call;
+
+/* n independent renderer calls issued together (1 <= n <= 4, one call per
+ * stage: the stages of the calls are distinct).  The result, the bank state
+ * afterwards and every error are those of calling ff_render_attn for
+ * calls[0], ..., calls[n-1] in order; since each call reads and writes only
+ * its own stage bank (and reads resident anchors), the calls do not depend on
+ * each other.  This is the single-GPU form of the pages' stage wavefront
+ * (onedev.kr/papers/332, "어떻게 동작하나": the S denoising stages work on
+ * different in-flight chunks at once, stage k on chunk i - k): the S calls of
+ * one layer at one wavefront step are independent.  All calls' RoPE/publish
+ * items run as one launch and all their query blocks as one attention launch,
+ * so the work of the calls is balanced across the SMs together.  Any error is
+ * found before any work is enqueued (FF_ERR_ARG also for n out of range or a
+ * repeated stage); the state is then unchanged. */
+int ff_render_attn_batch(ff_bank_t* bank, int n, const ff_render_call* calls, void* stream);
+
 /* Planner-role attention of planner block `block` of `layer`
  * (onedev.kr/papers/332, "무엇과 다른가": the planner produces the clean anchors
  * B_P = 3 at a time with history H_P = 6 and context budget W_ctx = 21;
@@ -219,14 +245,15 @@ int ff_plan_planner_block(const ff_bank_desc* desc, int block, ff_planner_plan* 
 /* ---- timing of the library's own kernels (CUDA events on the call's stream) ---- */
 
 typedef struct ff_kernel_times {
-  int calls;            /* ff_render_attn calls timed since the last reset */
-  double publish_ms;    /* summed duration of the RoPE + publish + gather kernel */
-  double attn_ms;       /* summed duration of the attention kernel */
-  double combine_ms;    /* summed duration of the split-combine kernel (0 when unsplit) */
+  int calls;            /* renderer calls timed since the last reset (a batch counts its calls) */
+  double publish_ms;    /* summed duration of the RoPE + publish launches */
+  double attn_ms;       /* summed duration of the attention launches */
+  double combine_ms;    /* summed duration of the split-combine launches (0 when unsplit) */
+  int launches;         /* kernels launched by the timed calls */
 } ff_kernel_times;
 
-/* enable != 0: record events around each kernel of subsequent render calls.
- * Resets the accumulated times. */
+/* enable != 0: record events around each kernel launch of subsequent renderer
+ * calls (ff_render_attn, ff_render_attn_batch).  Resets the accumulated times. */
 int ff_bank_set_timing(ff_bank_t* bank, int enable);
 
 /* Synchronise on the recorded events and return the accumulated times. */

@@ -132,9 +132,9 @@ struct TileCursor {
   }
 };
 
-template <int D, class P>
+template <int D, class P, class KV>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ KVMaps kv,
+    bank_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ KV kv,
                      const __grid_constant__ P p) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
-    for (int m = 0; m < kMaxMaps; ++m) {
+    for (int m = 0; m < KV::kMaps; ++m) {
       tma_prefetch_desc(&kv.k[m]);
       tma_prefetch_desc(&kv.v[m]);
     }
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (pc.part < 0) {
         const float inv = 1.0f / l_run;
         __nv_bfloat16* dst =
-            static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(G.q_row0 + lrow) * p.heads + head) * D;
+            static_cast<__nv_bfloat16*>(G.out) + (static_cast<size_t>(G.out_row0 + lrow) * p.heads + head) * D;
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
           float o[32];
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const 
   const int part = threadIdx.x % TPR;
   const int lrow = qb * 256 + rloc;
   if (lrow >= G.nq) return;
-  const int row = G.q_row0 + lrow;
+  const int row = G.out_row0 + lrow;
   const int ns = p.n_split;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   float2 mls[kMaxSplit];
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const 
     }
   }
   const float inv = 1.0f / l;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(row) * p.heads + head) * D + part * PER;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(G.out) + (static_cast<size_t>(row) * p.heads + head) * D + part * PER;
   uint32_t w[PER / 2];
 #pragma unroll
   for (int i = 0; i < PER / 2; ++i) w[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
@@ -558,66 +558,76 @@ size_t attention_smem_bytes(int head_dim) {
   return head_dim == 128 ? AttnCfg<128>::SMEM : AttnCfg<64>::SMEM;
 }
 
-cudaError_t attention_configure(int head_dim) {
-  cudaError_t e;
-  if (head_dim == 128) {
-    e = cudaFuncSetAttribute(bank_attn_kernel<128, AttnParamsN<1>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnCfg<128>::SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bank_attn_kernel<128, AttnParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               AttnCfg<128>::SMEM);
-  } else {
-    e = cudaFuncSetAttribute(bank_attn_kernel<64, AttnParamsN<1>>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnCfg<64>::SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bank_attn_kernel<64, AttnParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               AttnCfg<64>::SMEM);
-  }
+namespace {
+template <int D, class P, class KV>
+cudaError_t attn_attr() {
+  return cudaFuncSetAttribute(bank_attn_kernel<D, P, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              AttnCfg<D>::SMEM);
+}
+
+template <int D>
+cudaError_t attn_attr_all() {
+  cudaError_t e = attn_attr<D, AttnParamsN<1>, KVMaps>();
+  if (e == cudaSuccess) e = attn_attr<D, AttnParams, KVMaps>();
+  if (e == cudaSuccess) e = attn_attr<D, AttnParamsN<kMaxBatch>, KVMapsBatch>();
   return e;
 }
 
-namespace {
-// A copy of `p` sized for its single query group.
-AttnParamsN<1> single_group(const AttnParams& p) {
-  AttnParamsN<1> q{};
+// A copy of `p` sized for its first NG query groups.
+template <int NG>
+AttnParamsN<NG> first_groups(const AttnParams& p) {
+  AttnParamsN<NG> q{};
   static_cast<AttnHeader&>(q) = p;
-  q.groups[0] = p.groups[0];
+  for (int g = 0; g < NG && g < p.n_groups; ++g) q.groups[g] = p.groups[g];
   return q;
+}
+
+template <class P, class KV>
+void launch_attn_p(int head_dim, const CUtensorMap& tq, const KV& kv, const P& p, int grid, cudaStream_t s) {
+  if (head_dim == 128)
+    bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, p);
+  else
+    bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
+}
+
+template <class P>
+void launch_combine_p(int head_dim, const P& p, dim3 grid, cudaStream_t s) {
+  if (head_dim == 128)
+    attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
+  else
+    attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
 }
 }  // namespace
 
+cudaError_t attention_configure(int head_dim) {
+  return head_dim == 128 ? attn_attr_all<128>() : attn_attr_all<64>();
+}
+
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& kv, const AttnParams& p, int grid,
                              cudaStream_t s) {
-  if (p.n_groups == 1) {
-    const AttnParamsN<1> q = single_group(p);
-    if (head_dim == 128)
-      bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, q);
-    else
-      bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, q);
-  } else {
-    if (head_dim == 128)
-      bank_attn_kernel<128><<<grid, kAttnThreads, AttnCfg<128>::SMEM, s>>>(tq, kv, p);
-    else
-      bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
-  }
+  if (p.n_groups == 1)
+    launch_attn_p(head_dim, tq, kv, first_groups<1>(p), grid, s);
+  else
+    launch_attn_p(head_dim, tq, kv, p, grid, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMapsBatch& kv, const AttnParams& p,
+                             int grid, cudaStream_t s) {
+  if (p.n_groups > kMaxBatch) return cudaErrorInvalidValue;
+  launch_attn_p(head_dim, tq, kv, first_groups<kMaxBatch>(p), grid, s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
   // split units x 256 rows in blocks of 128 / (d / 8) rows
   dim3 grid(p.heads * p.n_qb - p.n_whole, 256 / (kCombineThreads / (head_dim / 8)));
-  if (p.n_groups == 1) {
-    const AttnParamsN<1> q = single_group(p);
-    if (head_dim == 128)
-      attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(q);
-    else
-      attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(q);
-  } else {
-    if (head_dim == 128)
-      attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
-    else
-      attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
-  }
+  if (p.n_groups == 1)
+    launch_combine_p(head_dim, first_groups<1>(p), grid, s);
+  else if (p.n_groups <= kMaxBatch)
+    launch_combine_p(head_dim, first_groups<kMaxBatch>(p), grid, s);
+  else
+    launch_combine_p(head_dim, p, grid, s);
   return cudaGetLastError();
 }
 

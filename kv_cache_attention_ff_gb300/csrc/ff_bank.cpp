@@ -68,6 +68,8 @@ struct SegSpec {
 struct TimedCall {
   cudaEvent_t ev[4];
   bool combine;
+  int calls;     // renderer calls the events cover (a batch covers several)
+  int launches;  // kernels launched between ev[0] and ev[3]
 };
 
 constexpr int kQBlock = 256;  // query rows per attention work unit
@@ -89,6 +91,7 @@ struct ff_bank {
 
   // device memory
   uint8_t* stage_kv = nullptr;   // [L][S][K, V][H + 1 slots][B_R frames]
+  uint8_t* q_rot_all = nullptr;  // [S][B_R frames]: every stage's rotated-Q scratch
   uint8_t* anchor_kv = nullptr;  // [L][K, V][cap][1 frame]
   struct Scratch {
     uint8_t* q_rot = nullptr;
@@ -290,12 +293,13 @@ int tiles_of(const std::vector<SegSpec>& seg, long long T) {
   return tiles;
 }
 
-// Fill group `g`'s key segments and the launch's K/V maps (one pair per
-// segment, each ending where its segment ends).  `base` gives each segment's
-// first K and V frame.
-template <class Base>
-int build_segments(const ff_bank* b, const std::vector<SegSpec>& seg, Base base, AttnGroup& g, KVMaps& kv) {
-  if (seg.empty() || seg.size() > static_cast<size_t>(kMaxSegs)) return FF_ERR_ARG;
+// Fill group `g`'s key segments and the launch's K/V maps m0, m0 + 1, ...
+// (one pair per segment, each ending where its segment ends).  `base` gives
+// each segment's first K and V frame.
+template <class Base, class KV>
+int build_segments(const ff_bank* b, const std::vector<SegSpec>& seg, Base base, AttnGroup& g, KV& kv, int m0 = 0) {
+  if (seg.empty() || seg.size() > static_cast<size_t>(kMaxSegs) || m0 + static_cast<int>(seg.size()) > KV::kMaps)
+    return FF_ERR_ARG;
   const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
   g.n_seg = 0;
   int tiles = 0;
@@ -304,23 +308,37 @@ int build_segments(const ff_bank* b, const std::vector<SegSpec>& seg, Base base,
     const void* v = nullptr;
     base(sp, &k, &v);
     const long long rows = sp.frames * T;
-    const int m = g.n_seg;
+    const int m = m0 + g.n_seg;
     int rc;
     if ((rc = make_map(b, &kv.k[m], k, static_cast<int>(rows))) != FF_OK) return rc;
     if ((rc = make_map(b, &kv.v[m], v, static_cast<int>(rows))) != FF_OK) return rc;
-    g.seg_map[m] = m;
-    g.seg_row0[m] = 0;
-    g.seg_rows[m] = static_cast<int>(rows);
-    g.seg_tile0[m] = tiles;
+    g.seg_map[g.n_seg] = m;
+    g.seg_row0[g.n_seg] = 0;
+    g.seg_rows[g.n_seg] = static_cast<int>(rows);
+    g.seg_tile0[g.n_seg] = tiles;
     tiles += static_cast<int>((rows + kKTile - 1) / kKTile);
     ++g.n_seg;
   }
   g.n_kv = tiles;
-  for (int m = g.n_seg; m < kMaxMaps; ++m) {  // unused entries stay valid descriptors
+  return FF_OK;
+}
+
+// Unused map entries of a launch stay valid descriptors (copies of entry 0,
+// which every launch uses): entries [used, kMaps), or those not marked in `used`.
+template <class KV>
+void fill_unused_maps(KV& kv, int used) {
+  for (int m = used; m < KV::kMaps; ++m) {
     kv.k[m] = kv.k[0];
     kv.v[m] = kv.v[0];
   }
-  return FF_OK;
+}
+template <class KV>
+void fill_unused_maps(KV& kv, const bool* used) {
+  for (int m = 1; m < KV::kMaps; ++m)
+    if (!used[m]) {
+      kv.k[m] = kv.k[0];
+      kv.v[m] = kv.v[0];
+    }
 }
 
 // Work plan and Q tensor map of an attention launch for the query groups in
@@ -335,7 +353,10 @@ int prepare_attention(const ff_bank* b, AttnParams& ap, const void* q, int q_row
   if (rc != FF_OK) return rc;
   const int units = b->d.heads * ap.n_qb;
   SplitPlan sp{units, 1, units, 0};
-  if (ap.n_groups == 1 && allow_split) sp = plan_split(units, ap.groups[0].n_kv, b->sm_count, part_rows);
+  // the planner's cost model assumes one key-tile count for every unit
+  bool uniform = true;
+  for (int g = 1; g < ap.n_groups; ++g) uniform = uniform && ap.groups[g].n_kv == ap.groups[0].n_kv;
+  if (allow_split && uniform) sp = plan_split(units, ap.groups[0].n_kv, b->sm_count, part_rows);
   ap.n_whole = sp.n_whole;
   ap.n_split = sp.n_split;
   ap.n_pieces = sp.n_pieces;
@@ -344,14 +365,18 @@ int prepare_attention(const ff_bank* b, AttnParams& ap, const void* q, int q_row
 
 // Launch attention (and the split combine) prepared by prepare_attention over
 // the K/V maps `kv`.  With `tc`, ev[2] is recorded between attention and combine.
-int attend(const ff_bank* b, const AttnParams& ap, const CUtensorMap& tq, const KVMaps& kv, cudaStream_t s,
+template <class KV>
+int attend(const ff_bank* b, const AttnParams& ap, const CUtensorMap& tq, const KV& kv, cudaStream_t s,
            TimedCall* tc) {
   int rc;
   const int grid = std::min(ap.n_pieces, b->sm_count);
   if ((rc = cuda_err(launch_attention(b->d.head_dim, tq, kv, ap, grid, s), "attention launch")) != FF_OK) return rc;
   if (tc) cudaEventRecord(tc->ev[2], s);
   if (ap.n_split > 1 && (rc = cuda_err(launch_combine(b->d.head_dim, ap, s), "combine launch")) != FF_OK) return rc;
-  if (tc) tc->combine = ap.n_split > 1;
+  if (tc) {
+    tc->combine = ap.n_split > 1;
+    tc->launches += ap.n_split > 1 ? 2 : 1;
+  }
   return FF_OK;
 }
 
@@ -374,14 +399,16 @@ G1Params publish_params(const ff_bank* b) {
   return prm;
 }
 
-G1Item rot_item(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int t, int q_frame) {
+G1Item rot_item(const void* src_k, const void* src_v, void* dst_k, void* dst_v, int t, const void* src_q = nullptr,
+                void* dst_q = nullptr) {
   G1Item it{};
   it.src_k = src_k;
   it.src_v = src_v;
+  it.src_q = src_q;
   it.dst_k = dst_k;
   it.dst_v = dst_v;
+  it.dst_q = dst_q;
   it.t = t;
-  it.q_frame = q_frame;
   return it;
 }
 
@@ -445,6 +472,8 @@ int next_timed_call(ff_bank* b, TimedCall** tc) {
   }
   *tc = &b->timed[b->n_timed];
   (*tc)->combine = false;
+  (*tc)->calls = 1;
+  (*tc)->launches = 0;
   return FF_OK;
 }
 
@@ -454,6 +483,166 @@ void wait_stage_events(ff_bank* b, cudaStream_t s, int only_stage) {
     if (only_stage >= 0 && k != only_stage) continue;
     if (b->stage_used[k] && b->stage_stream[k] != s) cudaStreamWaitEvent(s, b->ev_stage[k], 0);
   }
+}
+
+// One renderer call, checked and planned: everything about it that can fail
+// is found here, before any work is enqueued.
+struct RenderCall {
+  ff_render_call c;
+  ff_chunk_plan pl;
+  int aslots[2];
+  int own_phys;
+  std::vector<SegSpec> seg;
+};
+
+int check_render_call(const ff_bank* b, const ff_render_call& c, RenderCall* rc) {
+  const ff_bank_desc& d = b->d;
+  if (c.layer < 0 || c.layer >= d.n_layers || c.stage < 0 || c.stage >= d.n_stages || c.chunk < 0 ||
+      c.chunk >= n_chunks(d) || !c.q_pre || !c.k_pre || !c.v || !c.out || !aligned16(c.q_pre) || !aligned16(c.k_pre) ||
+      !aligned16(c.v) || !aligned16(c.out))
+    return FF_ERR_ARG;
+  if (c.chunk != b->next_chunk[static_cast<size_t>(c.layer) * d.n_stages + c.stage]) return FF_ERR_ORDER;
+  rc->c = c;
+  plan(d, c.chunk, &rc->pl);
+  const ff_chunk_plan& pl = rc->pl;
+  for (int j = 0; j < pl.n_anchors; ++j) {
+    rc->aslots[j] = (pl.anchors[j] / d.anchor_stride) % d.anchor_capacity;
+    if (b->aslot(c.layer, rc->aslots[j]).tag != pl.anchors[j]) return FF_ERR_ANCHOR_MISSING;
+  }
+  rc->own_phys = c.chunk % b->ring;
+  for (int jc = pl.hist_first; jc < c.chunk; ++jc)
+    if (b->sslot(c.layer, c.stage, jc % b->ring).tag != jc) return FF_ERR_ARG;  // internal invariant (Tail_H) broken
+  rc->seg = chunk_segments(d, c.chunk, pl);
+  int key_frames = 0;
+  for (const SegSpec& g : rc->seg) key_frames += g.frames;
+  return key_frames == pl.key_frames ? FF_OK : FF_ERR_ARG;
+}
+
+// The call's publish items: RoPE of its Q frames into `q_rot`, RoPE(K) and V
+// into its ring slot.
+void add_render_items(const ff_bank* b, const RenderCall& r, uint8_t* q_rot, G1Params& prm) {
+  const ff_render_call& c = r.c;
+  for (int f = 0; f < r.pl.n_frames; ++f)
+    prm.items[prm.n_items++] =
+        rot_item(frame_at(c.k_pre, f, b->frame_bytes), frame_at(c.v, f, b->frame_bytes),
+                 b->stage_k(c.layer, c.stage, r.own_phys) + static_cast<size_t>(f) * b->frame_bytes,
+                 b->stage_v(c.layer, c.stage, r.own_phys) + static_cast<size_t>(f) * b->frame_bytes,
+                 r.pl.first_frame + f, frame_at(c.q_pre, f, b->frame_bytes), q_rot + static_cast<size_t>(f) * b->frame_bytes);
+}
+
+// The call's query group: rows q_row0 .. of the launch's Q map, key segments
+// read in place through maps m0, m0 + 1, ...
+template <class KV>
+int add_render_group(const ff_bank* b, const RenderCall& r, int q_row0, int qb0, AttnGroup& g, KV& kv, int m0) {
+  const ff_render_call& c = r.c;
+  const long long T = static_cast<long long>(b->d.frame_h) * b->d.frame_w;
+  g.q_row0 = q_row0;
+  g.nq = static_cast<int>(r.pl.n_frames * T);
+  g.qb0 = qb0;
+  g.out = c.out;
+  g.out_row0 = 0;
+  return build_segments(b, r.seg,
+                        [&](const SegSpec& sg, const void** k, const void** vv) {
+                          *k = sg.plane == 0 ? b->anchor_k(c.layer, sg.slot) : b->stage_k(c.layer, c.stage, sg.slot);
+                          *vv = sg.plane == 0 ? b->anchor_v(c.layer, sg.slot) : b->stage_v(c.layer, c.stage, sg.slot);
+                        },
+                        g, kv, m0);
+}
+
+// Bank state after a call: its chunk is resident in its ring slot.
+void commit_render(ff_bank* b, const RenderCall& r) {
+  SlotState& own = b->sslot(r.c.layer, r.c.stage, r.own_phys);
+  own.tag = r.c.chunk;
+  own.frames = r.pl.n_frames;
+  ++b->next_chunk[static_cast<size_t>(r.c.layer) * b->d.n_stages + r.c.stage];
+}
+
+// n independent renderer calls (distinct stages when n > 1) as one RoPE/publish
+// launch and one attention launch (plus the split combine when planned).  Every
+// check runs before the first launch.
+int render_calls(ff_bank* b, int n, const ff_render_call* calls, cudaStream_t s) {
+  const ff_bank_desc& d = b->d;
+  RenderCall rcs[kMaxBatch];
+  int rc;
+  for (int j = 0; j < n; ++j) {
+    for (int i = 0; i < j; ++i)
+      if (calls[i].stage == calls[j].stage) return FF_ERR_ARG;  // one call per stage bank and scratch
+    if ((rc = check_render_call(b, calls[j], &rcs[j])) != FF_OK) return rc;
+  }
+  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
+  const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
+  const int slot_rows = static_cast<int>(d.chunk_frames * T);  // Q rows of one stage's scratch
+
+  G1Params prm = publish_params(b);
+  prm.n_items = 0;
+  AttnParams ap{};
+  ap.err = b->err;
+  ap.heads = d.heads;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
+  ap.n_groups = n;
+  KVMaps kv1;
+  KVMapsBatch kvb;
+  int qb = 0;
+  for (int j = 0; j < n; ++j) {
+    const RenderCall& r = rcs[j];
+    add_render_items(b, r, b->scratch[r.c.stage].q_rot, prm);
+    // every stage's Q scratch is a row range of one buffer: one Q map serves the batch
+    const int q_row0 = n == 1 ? 0 : r.c.stage * slot_rows;
+    rc = n == 1 ? add_render_group(b, r, q_row0, qb, ap.groups[j], kv1, 0)
+                : add_render_group(b, r, q_row0, qb, ap.groups[j], kvb, j * kMaxMaps);
+    if (rc != FF_OK) return rc;
+    qb += (ap.groups[j].nq + kQBlock - 1) / kQBlock;
+  }
+  ap.n_qb = qb;
+  if (n == 1) {
+    fill_unused_maps(kv1, static_cast<int>(rcs[0].seg.size()));
+  } else {
+    bool used[KVMapsBatch::kMaps] = {};
+    for (int j = 0; j < n; ++j)
+      for (size_t m = 0; m < rcs[j].seg.size(); ++m) used[j * kMaxMaps + m] = true;
+    fill_unused_maps(kvb, used);
+  }
+  // the first call's stage scratch holds the split partials of the launch
+  ff_bank::Scratch& sc = b->scratch[rcs[0].c.stage];
+  const void* q_map_base = n == 1 ? static_cast<const void*>(sc.q_rot) : static_cast<const void*>(b->q_rot_all);
+  const int q_map_rows = n == 1 ? rcs[0].pl.n_frames * static_cast<int>(T) : d.n_stages * slot_rows;
+  CUtensorMap tq;
+  if ((rc = prepare_attention(b, ap, q_map_base, q_map_rows, sc.part_o, sc.part_ml, b->part_rows, true, &tq)) != FF_OK)
+    return rc;
+  TimedCall* tc = nullptr;
+  if (b->timing && (rc = next_timed_call(b, &tc)) != FF_OK) return rc;
+
+  // ---- ordering against other streams
+  for (int j = 0; j < n; ++j) {
+    const RenderCall& r = rcs[j];
+    wait_stage_events(b, s, r.c.stage);
+    for (int a = 0; a < r.pl.n_anchors; ++a)
+      if (b->anchor_used[r.aslots[a]] && b->anchor_stream[r.aslots[a]] != s)
+        cudaStreamWaitEvent(s, b->ev_anchor[r.aslots[a]], 0);
+  }
+
+  // ---- nothing below fails for a reason that can be checked beforehand
+  if (tc) {
+    tc->calls = n;
+    tc->launches = 1;
+    cudaEventRecord(tc->ev[0], s);
+  }
+  if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
+  if (tc) cudaEventRecord(tc->ev[1], s);
+  rc = n == 1 ? attend(b, ap, tq, kv1, s, tc) : attend(b, ap, tq, kvb, s, tc);
+  if (rc != FF_OK) return rc;
+  if (tc) {
+    cudaEventRecord(tc->ev[3], s);
+    ++b->n_timed;
+  }
+  for (int j = 0; j < n; ++j) {
+    const int st = rcs[j].c.stage;
+    cudaEventRecord(b->ev_stage[st], s);
+    b->stage_stream[st] = s;
+    b->stage_used[st] = true;
+    commit_render(b, rcs[j]);
+  }
+  return FF_OK;
 }
 
 }  // namespace
@@ -584,9 +773,10 @@ int ff_bank_create(const ff_bank_desc* desc, ff_bank_t** out) {
   if ((rc = alloc(b, anchor_bytes, &p)) != FF_OK) goto fail;
   b->anchor_kv = static_cast<uint8_t*>(p);
   b->scratch.resize(d.n_stages);
+  if ((rc = alloc(b, qrot_bytes * d.n_stages, &p)) != FF_OK) goto fail;
+  b->q_rot_all = static_cast<uint8_t*>(p);
   for (int k = 0; k < d.n_stages; ++k) {
-    if ((rc = alloc(b, qrot_bytes, &p)) != FF_OK) goto fail;
-    b->scratch[k].q_rot = static_cast<uint8_t*>(p);
+    b->scratch[k].q_rot = b->q_rot_all + static_cast<size_t>(k) * qrot_bytes;
     if ((rc = alloc(b, part_o_bytes, &p)) != FF_OK) goto fail;
     b->scratch[k].part_o = static_cast<float*>(p);
     if ((rc = alloc(b, part_ml_bytes, &p)) != FF_OK) goto fail;
@@ -771,7 +961,7 @@ int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_p
     const int a = first + j * d.anchor_stride;
     const int sl = (a / d.anchor_stride) % d.anchor_capacity;
     prm.items[j] = rot_item(frame_at(k_pre, j, b->frame_bytes), frame_at(v, j, b->frame_bytes), b->anchor_k(layer, sl),
-                            b->anchor_v(layer, sl), a, -1);
+                            b->anchor_v(layer, sl), a);
   }
   // The slots may still be read by renders or planner blocks on other streams.
   wait_stage_events(b, s, -1);
@@ -792,90 +982,14 @@ int ff_anchor_publish(ff_bank_t* b, int layer, int first, int n, const void* k_p
 
 int ff_render_attn(ff_bank_t* b, int layer, int stage, int chunk, const void* q_pre, const void* k_pre, const void* v,
                    void* out, void* stream) {
-  if (!b || layer < 0 || layer >= b->d.n_layers || stage < 0 || stage >= b->d.n_stages || chunk < 0 ||
-      chunk >= n_chunks(b->d) || !q_pre || !k_pre || !v || !out || !aligned16(q_pre) || !aligned16(k_pre) ||
-      !aligned16(v) || !aligned16(out))
-    return FF_ERR_ARG;
-  const ff_bank_desc& d = b->d;
-  int& next = b->next_chunk[static_cast<size_t>(layer) * d.n_stages + stage];
-  if (chunk != next) return FF_ERR_ORDER;
-  ff_chunk_plan pl;
-  plan(d, chunk, &pl);
-  int aslots[2];
-  for (int j = 0; j < pl.n_anchors; ++j) {
-    aslots[j] = (pl.anchors[j] / d.anchor_stride) % d.anchor_capacity;
-    if (b->aslot(layer, aslots[j]).tag != pl.anchors[j]) return FF_ERR_ANCHOR_MISSING;
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaSetDevice(d.device) != cudaSuccess) return FF_ERR_CUDA;
-  ff_bank::Scratch& sc = b->scratch[stage];
-  const int own_phys = chunk % b->ring;
-  for (int jc = pl.hist_first; jc < chunk; ++jc)
-    if (b->sslot(layer, stage, jc % b->ring).tag != jc) return FF_ERR_ARG;  // internal invariant (Tail_H) broken
+  if (!b) return FF_ERR_ARG;
+  const ff_render_call c{layer, stage, chunk, q_pre, k_pre, v, out};
+  return render_calls(b, 1, &c, static_cast<cudaStream_t>(stream));
+}
 
-  // ---- RoPE + publish of the own chunk into its ring slot
-  G1Params prm = publish_params(b);
-  prm.q_in = q_pre;
-  prm.q_rot = sc.q_rot;
-  prm.n_items = pl.n_frames;
-  for (int r = 0; r < pl.n_frames; ++r)
-    prm.items[r] = rot_item(frame_at(k_pre, r, b->frame_bytes), frame_at(v, r, b->frame_bytes),
-                            b->stage_k(layer, stage, own_phys) + static_cast<size_t>(r) * b->frame_bytes,
-                            b->stage_v(layer, stage, own_phys) + static_cast<size_t>(r) * b->frame_bytes,
-                            pl.first_frame + r, r);
-
-  // ---- key segments, read in place: [anchor runs ; ring runs]
-  const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
-  const int nq = static_cast<int>(pl.n_frames * T);
-  AttnParams ap{};
-  ap.out = out;
-  ap.err = b->err;
-  ap.heads = d.heads;
-  attn_single_group(ap, nq, 0);
-  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
-  KVMaps kv;
-  const std::vector<SegSpec> seg = chunk_segments(d, chunk, pl);
-  int key_frames = 0;
-  for (const SegSpec& g : seg) key_frames += g.frames;
-  if (key_frames != pl.key_frames) return FF_ERR_ARG;
-  int rc = build_segments(b, seg,
-                          [&](const SegSpec& g, const void** k, const void** vv) {
-                            *k = g.plane == 0 ? b->anchor_k(layer, g.slot) : b->stage_k(layer, stage, g.slot);
-                            *vv = g.plane == 0 ? b->anchor_v(layer, g.slot) : b->stage_v(layer, stage, g.slot);
-                          },
-                          ap.groups[0], kv);
-  if (rc != FF_OK) return rc;
-
-  // ---- ordering against other streams
-  wait_stage_events(b, s, stage);
-  for (int j = 0; j < pl.n_anchors; ++j)
-    if (b->anchor_used[aslots[j]] && b->anchor_stream[aslots[j]] != s) cudaStreamWaitEvent(s, b->ev_anchor[aslots[j]], 0);
-
-  CUtensorMap tq;
-  if ((rc = prepare_attention(b, ap, sc.q_rot, nq, sc.part_o, sc.part_ml, b->part_rows, true, &tq)) != FF_OK) return rc;
-  TimedCall* tc = nullptr;
-  if (b->timing) {
-    if ((rc = next_timed_call(b, &tc)) != FF_OK) return rc;
-    cudaEventRecord(tc->ev[0], s);
-  }
-
-  // ---- nothing below fails for a reason that can be checked beforehand
-  if ((rc = cuda_err(launch_publish(prm, 0, s), "publish launch")) != FF_OK) return rc;
-  if (tc) cudaEventRecord(tc->ev[1], s);
-  if ((rc = attend(b, ap, tq, kv, s, tc)) != FF_OK) return rc;
-  if (tc) {
-    cudaEventRecord(tc->ev[3], s);
-    ++b->n_timed;
-  }
-  cudaEventRecord(b->ev_stage[stage], s);
-  b->stage_stream[stage] = s;
-  b->stage_used[stage] = true;
-
-  SlotState& own = b->sslot(layer, stage, own_phys);
-  own.tag = chunk;
-  own.frames = pl.n_frames;
-  ++next;
-  return FF_OK;
+int ff_render_attn_batch(ff_bank_t* b, int n, const ff_render_call* calls, void* stream) {
+  if (!b || !calls || n < 1 || n > kMaxBatch) return FF_ERR_ARG;
+  return render_calls(b, n, calls, static_cast<cudaStream_t>(stream));
 }
 
 int ff_plan_planner_block(const ff_bank_desc* d, int block, ff_planner_plan* out) {
@@ -906,21 +1020,19 @@ int ff_planner_attn(ff_bank_t* b, int layer, int block, const void* q_pre, const
 
   // RoPE of the block's Q, K, V into scratch; nothing is published
   G1Params prm = publish_params(b);
-  prm.q_in = q_pre;
-  prm.q_rot = sc.q_rot;
   prm.n_items = pl.n_anchors;
   for (int r = 0; r < pl.n_anchors; ++r)
     prm.items[r] = rot_item(frame_at(k_pre, r, b->frame_bytes), frame_at(v, r, b->frame_bytes),
                             sc.own_k + static_cast<size_t>(r) * b->frame_bytes,
-                            sc.own_v + static_cast<size_t>(r) * b->frame_bytes, (pl.first_anchor + r) * d.anchor_stride, r);
+                            sc.own_v + static_cast<size_t>(r) * b->frame_bytes, (pl.first_anchor + r) * d.anchor_stride,
+                            frame_at(q_pre, r, b->frame_bytes), sc.q_rot + static_cast<size_t>(r) * b->frame_bytes);
 
   const long long T = static_cast<long long>(d.frame_h) * d.frame_w;
   const int nq = static_cast<int>(pl.n_anchors * T);
   AttnParams ap{};
-  ap.out = out;
   ap.err = b->err;
   ap.heads = d.heads;
-  attn_single_group(ap, nq, 0);
+  attn_single_group(ap, nq, 0, out);
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.head_dim)));
   KVMaps kv;
   int rc = build_segments(b, planner_segments(d, pl),
@@ -975,8 +1087,6 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
 
   // 1. rotary encoding of every anchor and frame into the workspace (batches of kMaxItems frames)
   G1Params prm = publish_params(b);
-  prm.q_in = q_pre;
-  prm.q_rot = qrot;
   int rc;
   for (int f0 = 0; f0 < A + N; f0 += kMaxItems) {
     const int f1 = std::min(A + N, f0 + kMaxItems);
@@ -986,10 +1096,11 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       uint8_t* dv = vall + static_cast<size_t>(f) * b->frame_bytes;
       if (f < A)
         prm.items[n_items++] = rot_item(frame_at(anchor_k_pre, f, b->frame_bytes), frame_at(anchor_v, f, b->frame_bytes),
-                                        dk, dv, f * d.anchor_stride, -1);
+                                        dk, dv, f * d.anchor_stride);
       else
         prm.items[n_items++] = rot_item(frame_at(k_pre, f - A, b->frame_bytes), frame_at(v, f - A, b->frame_bytes), dk,
-                                        dv, f - A, f - A);
+                                        dv, f - A, frame_at(q_pre, f - A, b->frame_bytes),
+                                        qrot + static_cast<size_t>(f - A) * b->frame_bytes);
     }
     prm.n_items = n_items;
     if ((rc = cuda_err(launch_publish(prm, 0, s), "packed rope launch")) != FF_OK) return rc;
@@ -1000,7 +1111,6 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
   for (int c0 = 0; c0 < nc; c0 += kMaxGroups) {
     const int c1 = std::min(nc, c0 + kMaxGroups);
     AttnParams ap{};
-    ap.out = out;
     ap.err = b->err;
     ap.heads = d.heads;
     ap.n_split = 1;
@@ -1014,6 +1124,8 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
       g.q_row0 = static_cast<int>(pl.first_frame * T);
       g.nq = static_cast<int>(pl.n_frames * T);
       g.qb0 = qb;
+      g.out = out;
+      g.out_row0 = g.q_row0;
       qb += (g.nq + kQBlock - 1) / kQBlock;
       g.n_seg = 0;
       int tiles = 0;
@@ -1035,10 +1147,7 @@ int ff_packed_render_attn(ff_bank_t* b, const void* q_pre, const void* k_pre, co
     if ((rc = make_map(b, &kv.k[0], kall, static_cast<int>((A + N) * T))) != FF_OK ||
         (rc = make_map(b, &kv.v[0], vall, static_cast<int>((A + N) * T))) != FF_OK)
       return rc;
-    for (int m = 1; m < kMaxMaps; ++m) {
-      kv.k[m] = kv.k[0];
-      kv.v[m] = kv.v[0];
-    }
+    fill_unused_maps(kv, 1);
     CUtensorMap tq;
     if ((rc = prepare_attention(b, ap, qrot, static_cast<int>(N * T), nullptr, nullptr, 0, false, &tq)) != FF_OK ||
         (rc = attend(b, ap, tq, kv, s, nullptr)) != FF_OK)
@@ -1090,7 +1199,8 @@ int ff_bank_read_timing(ff_bank_t* b, ff_kernel_times* out) {
     out->publish_ms += a;
     out->attn_ms += c;
     out->combine_ms += tc.combine ? e : 0.0;
-    ++out->calls;
+    out->calls += tc.calls;
+    out->launches += tc.launches;
   }
   return FF_OK;
 }

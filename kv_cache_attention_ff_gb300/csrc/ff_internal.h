@@ -18,24 +18,23 @@ namespace ff {
 // heads of a token, sharing their rotary angles).  An item reads a K and a V
 // frame, rotates K under the published-K contract and writes both to their
 // destination frames (a stage-ring slot, an anchor slot or a scratch buffer);
-// with q_frame >= 0 it also rotates frame q_frame of the Q input into the same
-// frame of q_rot.
+// with src_q set it also rotates that Q frame into dst_q.
 
 struct G1Item {
   const void* src_k;  // K frame before rotary encoding
   const void* src_v;  // V frame
+  const void* src_q;  // Q frame before rotary encoding, or null
   void* dst_k;        // rotated K frame
   void* dst_v;        // V frame (copied)
+  void* dst_q;        // rotated Q frame (when src_q is set)
   int t;              // absolute latent frame (rotary time position)
-  int q_frame;        // frame of q_in / q_rot to rotate, -1: none
 };
 
 constexpr int kMaxItems = 160;
 constexpr int kFewItems = 8;  // launches with at most this many items use a small parameter block
+constexpr int kBatchItems = 32;  // a batch of renderer calls: at most 4 calls x 8 frames
 
 struct G1Header {
-  const void* q_in;   // [F * T, h, d] queries before rotary encoding (or null)
-  void* q_rot;        // [F * T, h, d]
   const double2* rope64;  // rotary (cos, sin) in fp64: [total_frames][pt], then [frame_h][py], then [frame_w][px]
   const float2* rope32;   // the same table rounded to fp32
   int y_base, x_base;     // first row-axis and column-axis entries
@@ -59,17 +58,19 @@ using G1Params = G1ParamsN<kMaxItems>;
 // ----------------------------------------------------------------- attention
 
 // Attention work is described as query groups, each a run of query rows with
-// its own list of key segments.  A segment is a row range of one of the K/V
-// tensor-map pairs the launch carries.  A renderer call is one group whose
-// segments are read in place: runs of adjacent anchor slots and runs of
-// adjacent stage-ring slots, each with its own map whose extent ends at the
-// segment (rows past it read as zeros).  A planner call adds its own block from
-// scratch; a packed block-causal forward has one group per chunk, all
-// segments in one workspace map.
+// its own list of key segments and its own output.  A segment is a row range
+// of one of the K/V tensor-map pairs the launch carries.  A renderer call is
+// one group whose segments are read in place: runs of adjacent anchor slots and
+// runs of adjacent stage-ring slots, each with its own map whose extent ends at
+// the segment (rows past it read as zeros).  A batch of independent renderer
+// calls is one group per call; a planner call adds its own block from scratch;
+// a packed block-causal forward has one group per chunk, all segments in one
+// workspace map.
 constexpr int kMaxGroups = 96;
 constexpr int kMaxSegs = 4;
 constexpr int kMaxMaps = 4;
 constexpr int kMaxSplit = 4;  // key ranges a split unit is cut into, at most
+constexpr int kMaxBatch = 4;  // renderer calls in one batched launch
 
 struct AttnGroup {
   int q_row0;              // first query row of the group
@@ -81,16 +82,21 @@ struct AttnGroup {
   int seg_rows[kMaxSegs];  // key rows of each segment
   int seg_tile0[kMaxSegs]; // first 128-key tile of each segment in the group's tile sequence
   int n_kv;                // tiles over all segments
+  int out_row0;            // row of `out` that query row q_row0 goes to
+  void* out;               // bf16 [rows, h, d] output of the group
 };
 
 // K and V tensor maps of a launch (bf16 [rows, heads * head_dim], 64 x 128 boxes).
-struct KVMaps {
-  CUtensorMap k[kMaxMaps];
-  CUtensorMap v[kMaxMaps];
+template <int M>
+struct KVMapsN {
+  static constexpr int kMaps = M;
+  CUtensorMap k[M];
+  CUtensorMap v[M];
 };
+using KVMaps = KVMapsN<kMaxMaps>;
+using KVMapsBatch = KVMapsN<kMaxMaps * kMaxBatch>;
 
 struct AttnHeader {
-  void* out;            // bf16 [query rows, h, d]
   float* part_o;        // [split pieces][256][d] unnormalised partial outputs
   float* part_ml;       // [split pieces][256][2] running max (log2 units) and sum
   unsigned int* err;    // device error word
@@ -117,8 +123,9 @@ struct AttnParamsN : AttnHeader {
 };
 using AttnParams = AttnParamsN<kMaxGroups>;
 
-// Fill `p` with the single group [0, nq) x one key segment [0, nk) of map 0.
-inline void attn_single_group(AttnParams& p, int nq, int nk) {
+// Fill `p` with the single group [0, nq) x one key segment [0, nk) of map 0,
+// output rows [0, nq) of `out`.
+inline void attn_single_group(AttnParams& p, int nq, int nk, void* out) {
   p.n_groups = 1;
   AttnGroup& g = p.groups[0];
   g.q_row0 = 0;
@@ -130,6 +137,8 @@ inline void attn_single_group(AttnParams& p, int nq, int nk) {
   g.seg_rows[0] = nk;
   g.seg_tile0[0] = 0;
   g.n_kv = (nk + 127) / 128;
+  g.out = out;
+  g.out_row0 = 0;
   p.n_qb = (nq + 255) / 256;
 }
 
@@ -185,6 +194,9 @@ inline SplitPlan plan_split(int units, int n_kv, int sms, size_t max_part_rows) 
 cudaError_t launch_publish(const G1Params& p, int grid, cudaStream_t s);
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMaps& kv, const AttnParams& p, int grid,
                              cudaStream_t s);
+// A batch launch: at most kMaxBatch groups over up to kMaxMaps * kMaxBatch map pairs.
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMapsBatch& kv, const AttnParams& p,
+                             int grid, cudaStream_t s);
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s);
 size_t attention_smem_bytes(int head_dim);
 cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t s);

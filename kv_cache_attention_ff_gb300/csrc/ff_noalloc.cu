@@ -124,9 +124,8 @@ extern "C" int ff_attention_noalloc(const void* q, const void* k, const void* v,
   if (rc != FF_OK) return rc;
 
   ff::AttnParams ap{};
-  ap.out = out;
   ap.heads = heads;
-  ff::attn_single_group(ap, nq, nk);
+  ff::attn_single_group(ap, nq, nk, out);
   const size_t max_part_rows = (FF_NOALLOC_SCRATCH_BYTES - kErrBytes) / (static_cast<size_t>(head_dim) * 4 + 8);
   const ff::SplitPlan sp = ff::plan_split(heads * n_qb, ap.groups[0].n_kv, sms, max_part_rows);
   ap.n_whole = sp.n_whole;

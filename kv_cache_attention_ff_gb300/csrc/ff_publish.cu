@@ -210,10 +210,9 @@ __global__ void __launch_bounds__(kPubThreads, PubBounds<G>::kMinBlocks)
   const uint4* src_v = static_cast<const uint4*>(I.src_v);
   uint4* dst_k = static_cast<uint4*>(I.dst_k);
   uint4* dst_v = static_cast<uint4*>(I.dst_v);
-  const bool with_q = I.q_frame >= 0;
-  const size_t q_base = with_q ? static_cast<size_t>(I.q_frame) * upf : 0;
-  const uint4* q_in = static_cast<const uint4*>(p.q_in) + q_base;
-  uint4* q_out = static_cast<uint4*>(p.q_rot) + q_base;
+  const bool with_q = I.src_q != nullptr;
+  const uint4* q_in = static_cast<const uint4*>(I.src_q);
+  uint4* q_out = static_cast<uint4*>(I.dst_q);
 
   const int uph = p.units_per_head;             // a power of two
   const int groups = p.units_per_row / (uph * G);  // head groups per token
@@ -272,17 +271,25 @@ void launch_publish_p(const P& p, int upf, int heads, cudaStream_t s) {
 }
 }  // namespace
 
+namespace {
+template <int N>
+void launch_publish_n(const G1Params& p, int upf, int heads, cudaStream_t s) {
+  G1ParamsN<N> q{};
+  static_cast<G1Header&>(q) = p;
+  for (int i = 0; i < p.n_items; ++i) q.items[i] = p.items[i];
+  launch_publish_p(q, upf, heads, s);
+}
+}  // namespace
+
 cudaError_t launch_publish(const G1Params& p, int /*grid_hint*/, cudaStream_t s) {
   const int upf = static_cast<int>(p.units_per_frame);
   const int heads = p.units_per_row / p.units_per_head;
-  if (p.n_items <= kFewItems) {
-    G1ParamsN<kFewItems> q{};
-    static_cast<G1Header&>(q) = p;
-    for (int i = 0; i < p.n_items; ++i) q.items[i] = p.items[i];
-    launch_publish_p(q, upf, heads, s);
-  } else {
+  if (p.n_items <= kFewItems)
+    launch_publish_n<kFewItems>(p, upf, heads, s);
+  else if (p.n_items <= kBatchItems)
+    launch_publish_n<kBatchItems>(p, upf, heads, s);
+  else
     launch_publish_p(p, upf, heads, s);
-  }
   return cudaGetLastError();
 }
 

@@ -25,7 +25,7 @@ EXPORTS = [
     "ff_bank_gamma", "ff_bank_slot_info", "ff_bank_bytes", "ff_bank_error_poll", "ff_status_string",
     "ff_plan_chunk", "ff_bank_set_timing", "ff_bank_read_timing", "ff_render_kernel_count",
     "ff_attention_noalloc", "ff_bank_wait_probe", "ff_planner_attn", "ff_plan_planner_block",
-    "ff_packed_workspace_bytes", "ff_packed_render_attn",
+    "ff_packed_workspace_bytes", "ff_packed_render_attn", "ff_render_attn_batch",
 ]
 
 
@@ -64,7 +64,13 @@ class PlannerPlan(ctypes.Structure):
 
 class KernelTimes(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_int), ("publish_ms", ctypes.c_double), ("attn_ms", ctypes.c_double),
-                ("combine_ms", ctypes.c_double)]
+                ("combine_ms", ctypes.c_double), ("launches", ctypes.c_int)]
+
+
+class RenderCall(ctypes.Structure):
+    _fields_ = [("layer", ctypes.c_int), ("stage", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("q_pre", ctypes.c_void_p), ("k_pre", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -99,6 +105,7 @@ def _lib():
         lib.ff_packed_workspace_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
         lib.ff_packed_render_attn.argtypes = [P, V, V, V, V, V, V, V, ctypes.c_size_t, V]
         lib.ff_plan_planner_block.argtypes = [ctypes.POINTER(BankDesc), I, ctypes.POINTER(PlannerPlan)]
+        lib.ff_render_attn_batch.argtypes = [P, I, ctypes.POINTER(RenderCall), V]
         for name in EXPORTS:
             if name != "ff_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -202,6 +209,23 @@ class Bank:
         _check(_lib().ff_render_attn(self.handle, layer, stage, chunk, _ptr(q_pre, shape, "q_pre"),
                                      _ptr(k_pre, shape, "k_pre"), _ptr(v, shape, "v"), _ptr(out, shape, "out"),
                                      _stream(stream, self.device)), "ff_render_attn")
+
+    def render_attn_batch(self, calls, stream=None):
+        """Independent renderer calls, one per stage, issued together.
+        `calls`: sequence of (layer, stage, chunk, q_pre, k_pre, v, out)."""
+        arr = (RenderCall * len(calls))()
+        for j, (layer, stage, chunk, q_pre, k_pre, v, out) in enumerate(calls):
+            frames = plan_chunk(self.desc, chunk).n_frames if 0 <= chunk < self.n_chunks else self.desc.chunk_frames
+            shape = (frames * self.T, self.desc.heads, self.desc.head_dim)
+            arr[j] = RenderCall(layer, stage, chunk, _ptr(q_pre, shape, "q_pre"), _ptr(k_pre, shape, "k_pre"),
+                                _ptr(v, shape, "v"), _ptr(out, shape, "out"))
+        _check(_lib().ff_render_attn_batch(self.handle, len(calls), arr, _stream(stream, self.device)),
+               "ff_render_attn_batch")
+
+    def render_attn_batch_raw(self, calls, stream_handle) -> int:
+        """Pointer-level batch: `calls` of (layer, stage, chunk, q_ptr, k_ptr, v_ptr, out_ptr); returns the status."""
+        arr = (RenderCall * len(calls))(*[RenderCall(*c) for c in calls])
+        return _lib().ff_render_attn_batch(self.handle, len(calls), arr, ctypes.c_void_p(stream_handle))
 
     def planner_attn(self, layer, block, q_pre, k_pre, v, out, stream=None):
         n = plan_planner_block(self.desc, block).n_anchors
