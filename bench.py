@@ -330,9 +330,11 @@ def run_gpu(args):
     sustained = "sw_power_cap" in (clocks.get("reasons") or []) and "bf16_tflops_sustained" in peaks
     bf16_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     bf16_label = "sustained (sw_power_cap active in the timed window)" if sustained else "burst"
-    attn_ms = kt.attn_ms / max(kt.calls, 1)
+    attn_ms = kt.attn_ms / max(kt.calls, 1)      # per call
     pub_ms = kt.publish_ms / max(kt.calls, 1)
     comb_ms = kt.combine_ms / max(kt.calls, 1)
+    n_launch = math.ceil(args.steps / max(1, args.batch))  # attention (and publish) launches in the timed region
+    per_launch = kt.calls / max(n_launch, 1)                # calls one launch covers
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     pub_gbs = g1_bytes / (pub_ms * 1e-3) / 1e9
     roofline = {"kernel": "bank_attn_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
@@ -345,7 +347,8 @@ def run_gpu(args):
                                       if "bf16_tflops_sustained" in peaks else None),
                 "frac_of_datasheet": round(attn_tflops / DATASHEET_BF16_TFLOPS, 4),
                 "datasheet_peak": DATASHEET_BF16_TFLOPS,
-                "algorithmic_per_launch": f"{flops / 1e9:.1f} GFLOP (4*Nq*Nk*d*h)", "avg_launch_ms": round(attn_ms, 4)}
+                "algorithmic_per_launch": f"{per_launch * flops / 1e9:.1f} GFLOP ({per_launch:g} calls x 4*Nq*Nk*d*h)",
+                "avg_launch_ms": round(attn_ms * per_launch, 4)}
     pub_traffic = ncu_traffic("rope_publish_kernel")
     roofline_publish = {"kernel": "rope_publish_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
@@ -353,12 +356,14 @@ def run_gpu(args):
                         "traffic": pub_traffic, "traffic_unit": "bytes/launch",
                         "dram_gbs": round(pub_traffic / (pub_ms * 1e-3) / 1e9, 1) if pub_traffic else None,
                         "peak_source": f"{peak_src} hbm_gbs",
-                        "algorithmic_per_launch": f"{g1_bytes / 1e6:.1f} MB (18 frames x 4.79 MB)",
-                        "avg_launch_ms": round(pub_ms, 4)}
+                        "algorithmic_per_launch": f"{per_launch * g1_bytes / 1e6:.1f} MB ({per_launch:g} calls x "
+                                                  f"18 frames x 4.79 MB)",
+                        "avg_launch_ms": round(pub_ms * per_launch, 4)}
 
     # end to end: pinned host inputs -> device, call, output -> pinned host, every step
     e2e = None if args.no_e2e else run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev)
 
+    single = None if (args.no_e2e or args.batch <= 1) else run_single_calls(pool, stream, args, dev, flops)
     planner = None if args.no_e2e else run_planner(stream, args, dev)
     packed = None if args.no_e2e else run_packed(stream, args, dev)
     schedule = None if args.no_e2e else run_schedule(pool, stream, args, dev)
@@ -383,15 +388,62 @@ def run_gpu(args):
             "pct_bf16_peak": round(100 * value / peaks[bf16_key], 2),
             "pct_bf16_datasheet": round(100 * value / DATASHEET_BF16_TFLOPS, 2),
             "chunk_steps_per_s": round(1000.0 / (ms_step * LAYERS_PER_CHUNK_STEP) * world, 3),
-            "kernel_ms": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
+            "kernel_ms_per_call": {"rope_publish": round(pub_ms, 4), "attention": round(attn_ms, 4),
                           "combine": round(comb_ms, 4)},
             "roofline": roofline, "roofline_publish": roofline_publish,
-            "e2e": e2e, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kt.launches, "clocks": clocks,
+            "e2e": e2e, "single_call": single, "planner": planner, "packed": packed, "schedule": schedule, "configs_14b": configs, "cache_update_baselines": baselines, "gpu_launches": kt.launches, "clocks": clocks,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def run_single_calls(pool, stream, args, dev, flops):
+    """The headline's steady calls issued one ff_render_attn at a time (no
+    wavefront batching): each call splits its query blocks' key ranges to fill
+    the SMs and merges them with the combine kernel."""
+    import torch
+
+    from kv_cache_attention_ff_gb300 import ff
+    T, H, D = 1560, 12, 128
+    n = max(8, min(args.steps, 400))
+    warm = 4
+    layers = max(1, math.ceil((n + warm) / 88))
+    sb = ff.Bank(n_layers=layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
+                 total_frames=81, heads=H, head_dim=D, frame_h=30, frame_w=52, device=dev.index)
+    z = torch.zeros((3 * T, H, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(z)
+    for layer in range(layers):
+        for b in range(3):
+            sb.anchor_publish(layer, 30 * b, 3, z, z, stream)
+        for st in range(4):
+            for i in range(5):
+                sb.render_attn(layer, st, i, *pool[st][i % 4], out, stream)
+    calls = [(l, st, i) for i in range(5, 27) for l in range(layers) for st in range(4)][:n + warm]
+    for l, st, i in calls[:warm]:
+        sb.render_attn(l, st, i, *pool[st][i % 4], out, stream)
+    torch.cuda.synchronize()
+    sb.set_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for l, st, i in calls[warm:]:
+        q, k, v = pool[st][i % 4]
+        rc = sb.render_attn_raw(l, st, i, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"ff_render_attn failed with status {rc}")
+    e1.record(stream)
+    torch.cuda.synchronize()
+    kt = sb.read_timing()
+    sb.set_timing(False)
+    assert sb.error_poll() == 0
+    sb.close()
+    ms = e0.elapsed_time(e1) / n
+    c = max(kt.calls, 1)
+    return {"workload": "the headline's steady calls, one ff_render_attn each", "calls": n,
+            "ms_per_call": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "kernel_ms": {"rope_publish": round(kt.publish_ms / c, 4), "attention": round(kt.attn_ms / c, 4),
+                          "combine": round(kt.combine_ms / c, 4)}, "launches": kt.launches}
 
 
 def run_planner(stream, args, dev):
@@ -494,9 +546,11 @@ def run_baselines(pool, stream, args, dev, flops):
 def run_schedule(pool, stream, args, dev):
     """The full 81-latent schedule of the 1.3B 480p shape on one GPU: anchors
     published first (3 planner blocks of 3 per layer), then 27 chunks x 4 stages
-    x 30 layers of renderer calls in chunk-step order (chunk i, stage k, all
-    layers), ramp-up chunks included.  Inputs cycle the pool (time does not
-    depend on values)."""
+    x 30 layers of renderer calls in stage-wavefront order: at step w, every
+    layer renders chunk w - k at stage k (the pages' wavefront on one GPU),
+    ramp-up and drain steps included; with --batch > 1 the calls of one layer
+    at one step go out as one ff_render_attn_batch.  Inputs cycle the pool
+    (time does not depend on values)."""
     import torch
 
     from kv_cache_attention_ff_gb300 import ff, synth
@@ -517,11 +571,16 @@ def run_schedule(pool, stream, args, dev):
         for b in range(3):
             sb.anchor_publish(layer, 30 * b, 3, blocks[b][0], blocks[b][1], stream)
     e1.record(stream)
-    for i in range(27):
-        for st in range(4):
-            q, k, v = pool[st][i % 4]
-            for layer in range(L):
-                sb.render_attn(layer, st, i, q, k, v, out, stream)
+    outs = [torch.empty((3 * T, H, D), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    for w in range(27 + 3):
+        step = [(st, w - st) for st in range(4) if 0 <= w - st < 27]
+        for layer in range(L):
+            calls = [(layer, st, i, *pool[st][i % 4], outs[st]) for st, i in step]
+            if args.batch > 1:
+                sb.render_attn_batch(calls, stream)
+            else:
+                for c in calls:
+                    sb.render_attn(*c, stream)
     e2.record(stream)
     torch.cuda.synchronize()
     assert sb.error_poll() == 0
@@ -531,7 +590,8 @@ def run_schedule(pool, stream, args, dev):
     sb.close()
     render_s = e1.elapsed_time(e2) / 1e3
     flops = 4.0 * (3 * T) * (key_frames * T) * D * H * 4 * L
-    return {"workload": "1.3B 480p full schedule: 27 chunks x 4 stages x 30 layers, anchors published first",
+    return {"workload": "1.3B 480p full schedule: 27 chunks x 4 stages x 30 layers in stage-wavefront order, "
+                        "anchors published first", "calls_per_launch": args.batch,
             "renderer_calls": 27 * 4 * L, "key_frames_per_layer_stage": key_frames,
             "anchor_publish_ms": round(e0.elapsed_time(e1), 3), "render_ms": round(1e3 * render_s, 2),
             "chunk_steps_per_s": round(27 * 4 / render_s, 2), "tflops": round(flops / render_s / 1e12, 1)}
@@ -638,18 +698,22 @@ def run_packed(stream, args, dev):
 def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
     """Same calls through the public API with host buffers.  Every step copies
     its q, k, v from pinned host memory to the device and its output back to
-    pinned host memory inside the timed region.  Copies run on their own
-    streams with double-buffered device staging, so step j+1's upload and
-    step j-1's download overlap step j's kernels."""
+    pinned host memory inside the timed region.  Calls are issued like the
+    device-timed region (one ff_render_attn per call, or stage-wavefront
+    batches of --batch calls); copies run on their own streams with
+    double-buffered device staging per group of calls, so the next group's
+    upload and the previous group's download overlap a group's kernels."""
     import torch
 
     from kv_cache_attention_ff_gb300 import ff
     T, H, D = 1560, 12, 128
     nq = 3 * T
+    B = max(1, args.batch)
     host_in = [[t.cpu().pin_memory() for t in pool[s][0]] for s in range(4)]
-    host_out = [torch.empty((nq, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dbuf = [[torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)] for _ in range(2)]
-    dout = [torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    host_out = [[torch.empty((nq, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(B)] for _ in range(2)]
+    dbuf = [[[torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)] for _ in range(B)]
+            for _ in range(2)]
+    dout = [[torch.empty((nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(B)] for _ in range(2)]
     steps, warm = args.steps, args.warmup
     layers = max(1, math.ceil((steps + warm) / 88))
     eb = ff.Bank(n_layers=layers, n_stages=4, history=5, chunk_frames=3, anchor_stride=10, anchor_capacity=9,
@@ -677,39 +741,49 @@ def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
     computed = [ev(), ev()]
     downloaded = [ev(), ev()]
     started = [False, False]
+    groups = [(j, min(warm, j + B)) for j in range(0, warm, B)]
+    groups += [(j, min(warm + steps, j + B)) for j in range(warm, warm + steps, B)]
 
-    def step(j):
-        b = j & 1
-        layer, st, c = calls[j]
+    def group(g, j0, j1):
+        b = g & 1
         if started[b]:
-            up.wait_event(computed[b])          # staging buffer b is free once step j-2 ran
+            up.wait_event(computed[b])          # staging set b is free once group g-2 ran
         with torch.cuda.stream(up):
-            for dst, src in zip(dbuf[b], host_in[st]):
-                dst.copy_(src, non_blocking=True)
+            for slot, j in enumerate(range(j0, j1)):
+                for dst, src in zip(dbuf[b][slot], host_in[calls[j][1]]):
+                    dst.copy_(src, non_blocking=True)
             uploaded[b].record(up)
         stream.wait_event(uploaded[b])
         if started[b]:
-            stream.wait_event(downloaded[b])    # output buffer b was read back
-        dq, dk, dv = dbuf[b]
-        rc = eb.render_attn_raw(layer, st, c, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dout[b].data_ptr(),
-                                stream.cuda_stream)
+            stream.wait_event(downloaded[b])    # output set b was read back
+        args_list = []
+        for slot, j in enumerate(range(j0, j1)):
+            layer, st, c = calls[j]
+            dq, dk, dv = dbuf[b][slot]
+            args_list.append((layer, st, c, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dout[b][slot].data_ptr()))
+        if B == 1:
+            rc = eb.render_attn_raw(*args_list[0], stream.cuda_stream)
+        else:
+            rc = eb.render_attn_batch_raw(args_list, stream.cuda_stream)
         if rc != 0:
-            raise RuntimeError(f"ff_render_attn failed with status {rc}")
+            raise RuntimeError(f"renderer call failed with status {rc}")
         computed[b].record(stream)
         down.wait_event(computed[b])
         with torch.cuda.stream(down):
-            host_out[b].copy_(dout[b], non_blocking=True)
+            for slot in range(j1 - j0):
+                host_out[b][slot].copy_(dout[b][slot], non_blocking=True)
             downloaded[b].record(down)
         started[b] = True
 
-    for j in range(warm):
-        step(j)
+    n_warm_groups = len([1 for j0, _ in groups if j0 < warm])
+    for g in range(n_warm_groups):
+        group(g, *groups[g])
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(up)
-    for j in range(warm, warm + steps):
-        step(j)
+    for g in range(n_warm_groups, len(groups)):
+        group(g, *groups[g])
     e1.record(down)  # every upload precedes its kernels, which precede the download on `down`
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
@@ -717,7 +791,8 @@ def run_e2e(bank, n_layers, seq, pool, out, stream, args, flops, dev):
     bytes_in = 3 * nq * H * D * 2
     return {"value": round(flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_in,
             "d2h_bytes_per_step": nq * H * D * 2, "ms_per_step": round(ms / steps, 4),
-            "copies": "pinned host <-> device every step, double-buffered on two copy streams"}
+            "copies": "pinned host <-> device every step, double-buffered on two copy streams",
+            "calls_per_launch": B}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -841,7 +916,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass (profiling runs)")
     ap.add_argument("--stage-streams", type=int, default=1,
                     help="CUDA streams the 4 stages are issued on (1..4); per-kernel event times need 1")
-    ap.add_argument("--batch", type=int, default=1,
+    ap.add_argument("--batch", type=int, default=4,
                     help="calls per ff_render_attn_batch (1 = one ff_render_attn per step; 2..4 = stage wavefront "
                          "batches of consecutive calls, which have distinct stages)")
     args = ap.parse_args()

@@ -84,13 +84,15 @@ def test_wan13b_480p_full_schedule_sampled(ff):
     bank.close()
 
 
-def test_wan14b_720p_rollout_constant_memory(ff):
-    """261 latents = 87 chunks x 4 stages at 40 heads x 3600 tokens/frame, anchors published
-    per planner block on demand into a 6-slot ring; bank bytes and device free memory stay
-    constant over the rollout; stage 0 checked: published K/V bytes at sampled chunks and
-    attention on sampled rows of 4 heads at the last chunk."""
+def _rollout_720p(ff, n_layers, layers):
+    """261 latents = 87 chunks x 4 stages at 40 heads x 3600 tokens/frame, anchors
+    published per planner block on demand into a 6-slot ring, rendered at the given
+    layers of an n_layers-deep bank; bank bytes and device free memory stay constant
+    over the rollout; stage 0 of every rendered layer checked: published K/V bytes at
+    sampled chunks and attention on sampled rows of 4 heads at the last chunk."""
     from kv_cache_attention_ff_gb300 import synth
     cfg_id, fields, mode = CONFIGS["wan14b_720p_rollout"]
+    fields = dict(fields, n_layers=n_layers)
     T, h, d = 3600, fields["heads"], fields["head_dim"]
     N = fields["total_frames"]
     dev = torch.device("cuda:0")
@@ -108,66 +110,86 @@ def test_wan14b_720p_rollout_constant_memory(ff):
         av.f = f
         if f % 10 == 0:
             anchor_v[f] = av.next()
-    streams = [[synth.DeviceARStream(cfg_id, 0, st, t, T, h, d, mode if t < 2 else "normal")
-                for t in (synth.Q, synth.K, synth.V)] for st in range(4)]
     out = torch.empty((3 * T, h, d), dtype=torch.bfloat16, device=dev)
-    published = set()
-    hist = {}       # stage-0 chunk -> (k bits, v bits) of the checked heads
     chk_chunks = {0, 1, 2, 43, 86}
     rng = np.random.default_rng(5)
-    for i in range(87):
-        for a in fo.gamma(i, 3, 10, N):
-            blk = a // 30
-            if blk not in published:
-                frames = [f for f in (30 * blk, 30 * blk + 10, 30 * blk + 20) if f < N]
-                kk = torch.cat([anchor_k[f] for f in frames])
-                vv = torch.cat([anchor_v[f] for f in frames])
-                bank.anchor_publish(0, 30 * blk, len(frames), kk, vv)
-                published.add(blk)
-        s, e = fo.chunk_span(i, 3, N)
-        for st in range(4):
-            q, k, v = (x.frames(3) for x in streams[st])
-            torch.cuda.synchronize()
-            free_a = torch.cuda.mem_get_info(dev)[0]
-            bank.render_attn(0, st, i, q, k, v, out)
-            torch.cuda.synchronize()
-            free_b = torch.cuda.mem_get_info(dev)[0]
-            assert free_a == free_b, "the library allocated device memory during a render"
-            assert bank.bytes() == bytes0
-            if st != 0:
-                continue
-            kb, vb = to_bits(k), to_bits(v)
-            hist[i] = (kb[:, heads_chk], vb[:, heads_chk])
-            hist.pop(i - 6, None)
-            if i in chk_chunks:
-                pos = fo.token_positions(list(range(s, e + 1)), 45, 80)
-                k_rot = fo.rope_k_bits(kb, pos, d, 10000.0)
-                tag, sk, sv = bank.slot_tensors(0, 0, i % 5)
-                assert tag == i and np.array_equal(to_bits(sk), k_rot) and np.array_equal(to_bits(sv), vb)
-            if i == 86:
-                ks, vs = [], []
-                for a in fo.gamma(i, 3, 10, N):
-                    pa = fo.token_positions([a], 45, 80)
-                    ks.append(fo.rope_k_bits(to_bits(anchor_k[a])[:, heads_chk], pa, d, 10000.0))
-                    vs.append(to_bits(anchor_v[a])[:, heads_chk])
-                for j in range(i - 5, i + 1):
-                    js, je = fo.chunk_span(j, 3, N)
-                    pj = fo.token_positions(list(range(js, je + 1)), 45, 80)
-                    ks.append(fo.rope_k_bits(hist[j][0], pj, d, 10000.0))
-                    vs.append(hist[j][1])
-                K = fo.bf16_bits_to_f64(np.concatenate(ks))
-                V = fo.bf16_bits_to_f64(np.concatenate(vs))
-                assert K.shape[0] == 72000
-                Q = fo.rope_q_f64(to_bits(q)[:, heads_chk], fo.token_positions(list(range(s, e + 1)), 45, 80), d,
-                                  10000.0)
-                rows = _rows(Q.shape[0], 40, rng)
-                ref = fo.attention_rows_f64(Q, K, V, rows)
-                got = out[torch.from_numpy(rows).to(dev)][:, torch.from_numpy(heads_chk).to(dev)]
-                mae, rl2, ok = compare_out(got, ref)
-                assert ok, (mae, rl2)
-    assert len(published) == 9
+    for layer in layers:
+        streams = [[synth.DeviceARStream(cfg_id, layer, st, t, T, h, d, mode if t < 2 else "normal")
+                    for t in (synth.Q, synth.K, synth.V)] for st in range(4)]
+        published = set()
+        hist = {}       # stage-0 chunk -> (k bits, v bits) of the checked heads
+        for i in range(87):
+            for a in fo.gamma(i, 3, 10, N):
+                blk = a // 30
+                if blk not in published:
+                    frames = [f for f in (30 * blk, 30 * blk + 10, 30 * blk + 20) if f < N]
+                    kk = torch.cat([anchor_k[f] for f in frames])
+                    vv = torch.cat([anchor_v[f] for f in frames])
+                    bank.anchor_publish(layer, 30 * blk, len(frames), kk, vv)
+                    published.add(blk)
+            s, e = fo.chunk_span(i, 3, N)
+            for st in range(4):
+                q, k, v = (x.frames(3) for x in streams[st])
+                torch.cuda.synchronize()
+                free_a = torch.cuda.mem_get_info(dev)[0]
+                bank.render_attn(layer, st, i, q, k, v, out)
+                torch.cuda.synchronize()
+                free_b = torch.cuda.mem_get_info(dev)[0]
+                assert free_a == free_b, "the library allocated device memory during a render"
+                assert bank.bytes() == bytes0
+                if st != 0:
+                    continue
+                kb, vb = to_bits(k), to_bits(v)
+                hist[i] = (kb[:, heads_chk], vb[:, heads_chk])
+                hist.pop(i - 6, None)
+                if i in chk_chunks:
+                    pos = fo.token_positions(list(range(s, e + 1)), 45, 80)
+                    k_rot = fo.rope_k_bits(kb, pos, d, 10000.0)
+                    tag, sk, sv = bank.slot_tensors(layer, 0, i % 5)
+                    assert tag == i and np.array_equal(to_bits(sk), k_rot) and np.array_equal(to_bits(sv), vb)
+                if i == 86:
+                    ks, vs = [], []
+                    for a in fo.gamma(i, 3, 10, N):
+                        pa = fo.token_positions([a], 45, 80)
+                        ks.append(fo.rope_k_bits(to_bits(anchor_k[a])[:, heads_chk], pa, d, 10000.0))
+                        vs.append(to_bits(anchor_v[a])[:, heads_chk])
+                    for j in range(i - 5, i + 1):
+                        js, je = fo.chunk_span(j, 3, N)
+                        pj = fo.token_positions(list(range(js, je + 1)), 45, 80)
+                        ks.append(fo.rope_k_bits(hist[j][0], pj, d, 10000.0))
+                        vs.append(hist[j][1])
+                    K = fo.bf16_bits_to_f64(np.concatenate(ks))
+                    V = fo.bf16_bits_to_f64(np.concatenate(vs))
+                    assert K.shape[0] == 72000
+                    Q = fo.rope_q_f64(to_bits(q)[:, heads_chk], fo.token_positions(list(range(s, e + 1)), 45, 80), d,
+                                      10000.0)
+                    rows = _rows(Q.shape[0], 40, rng)
+                    ref = fo.attention_rows_f64(Q, K, V, rows)
+                    got = out[torch.from_numpy(rows).to(dev)][:, torch.from_numpy(heads_chk).to(dev)]
+                    mae, rl2, ok = compare_out(got, ref)
+                    assert ok, (layer, mae, rl2)
+        assert len(published) == 9
     assert bank.error_poll() == 0
+    nbytes = bank.bytes()
     bank.close()
+    return nbytes
+
+
+def test_wan14b_720p_rollout_constant_memory(ff):
+    _rollout_720p(ff, 1, (0,))
+
+
+def test_wan14b_720p_rollout_40_layer_bank(ff):
+    """The 14B 720p bank at full depth: 40 layers x 4 stages of H + 1 = 6 ring slots of
+    3 frames (K and V) plus 40 layers x 6 anchor slots; the rollout runs at layers 0
+    and 39 with constant device memory at every call."""
+    frame = 3600 * 40 * 128 * 2
+    rings = 40 * 4 * 6 * 2 * 3 * frame
+    anchors = 40 * 6 * 2 * frame
+    assert (rings, anchors) == (212_336_640_000, 17_694_720_000)
+    nbytes = _rollout_720p(ff, 40, (0, 39))
+    scratch = nbytes - rings - anchors    # per-stage rotated-Q scratch and split partials, planner scratch, tables
+    assert 0 < scratch < 2_000_000_000, scratch
 
 
 def test_stage_streams_match_single_stream(ff):
