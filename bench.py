@@ -35,24 +35,25 @@ WORKLOAD = "wan13b_480p"   # 12 heads, d 128, 30x52 tokens/frame, chunk 3 frames
 LAYERS_PER_CHUNK_STEP = 30  # Wan2.1-1.3B transformer blocks: a chunk-step runs every layer once
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the
-# steady call (profiles/*_wan13b_480p.md), with the source digest the counters belong to:
-# a kernel edited since then reports null.
+# steady 1.3B call issued as a batch of 4 calls (profiles/*_wan13b_480p.md), with the
+# source digest the counters belong to and the calls the captured launch covered: a
+# kernel edited since then, or a launch of another size, reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (221.1e6, "ff_attn.cu", "16db896386b0d636"),
-    "rope_publish_kernel": (45.3e6, "ff_publish.cu", "a28235a92b5440a1"),
+    "bank_attn_kernel": (838.5e6, "ff_attn.cu", "505a5239f142b753", 4),
+    "rope_publish_kernel": (288.6e6, "ff_publish.cu", "f39c3097d7c98795", 4),
 }
 
 
-def ncu_traffic(kernel):
+def ncu_traffic(kernel, calls_per_launch):
     import hashlib
-    nbytes, src, digest = NCU_TRAFFIC[kernel]
+    nbytes, src, digest, calls = NCU_TRAFFIC[kernel]
     path = os.path.join(ROOT, "kv_cache_attention_ff_gb300", "csrc", src)
     try:
         with open(path, "rb") as f:
             now = hashlib.sha256(f.read()).hexdigest()[:16]
     except OSError:
         return None
-    return nbytes if now == digest else None
+    return nbytes if now == digest and calls == calls_per_launch else None
 
 
 def load_peaks():
@@ -339,7 +340,7 @@ def run_gpu(args):
     pub_gbs = g1_bytes / (pub_ms * 1e-3) / 1e9
     roofline = {"kernel": "bank_attn_kernel", "bound": "tensor", "achieved": round(attn_tflops, 1),
                 "peak": peaks[bf16_key], "unit": "TFLOP/s", "frac": round(attn_tflops / peaks[bf16_key], 4),
-                "traffic": ncu_traffic("bank_attn_kernel"), "traffic_unit": "bytes/launch",
+                "traffic": ncu_traffic("bank_attn_kernel", per_launch), "traffic_unit": "bytes/launch",
                 "peak_source": f"{peak_src} {bf16_key} ({bf16_label})",
                 # the same launch against every denominator, side by side
                 "frac_of_burst": round(attn_tflops / peaks["bf16_tflops"], 4),
@@ -349,12 +350,12 @@ def run_gpu(args):
                 "datasheet_peak": DATASHEET_BF16_TFLOPS,
                 "algorithmic_per_launch": f"{per_launch * flops / 1e9:.1f} GFLOP ({per_launch:g} calls x 4*Nq*Nk*d*h)",
                 "avg_launch_ms": round(attn_ms * per_launch, 4)}
-    pub_traffic = ncu_traffic("rope_publish_kernel")
+    pub_traffic = ncu_traffic("rope_publish_kernel", per_launch)
     roofline_publish = {"kernel": "rope_publish_kernel", "bound": "hbm", "achieved": round(pub_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(pub_gbs / peaks["hbm_gbs"], 4),
                         "achieved_is": "effective bandwidth: algorithmic bytes / launch time (its writes stay in L2)",
                         "traffic": pub_traffic, "traffic_unit": "bytes/launch",
-                        "dram_gbs": round(pub_traffic / (pub_ms * 1e-3) / 1e9, 1) if pub_traffic else None,
+                        "dram_gbs": round(pub_traffic / (pub_ms * per_launch * 1e-3) / 1e9, 1) if pub_traffic else None,
                         "peak_source": f"{peak_src} hbm_gbs",
                         "algorithmic_per_launch": f"{per_launch * g1_bytes / 1e6:.1f} MB ({per_launch:g} calls x "
                                                   f"18 frames x 4.79 MB)",
