@@ -10,6 +10,8 @@ against a brute force over explicitly named frames
 section "어떻게 동작하나", Eq. (2): chunk i reads B_k^(i) (anchors of Gamma(i),
 the last H same-stage chunks) and then leaves B_k^(i+1) = Tail_H(B_k^(i) U (i, K, V)).
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -132,3 +134,49 @@ def test_token_positions_hand_values():
     # a frame 3 rows x 5 columns, every token by hand
     p = fo.token_positions([0], 3, 5)
     assert [tuple(r[1:]) for r in p] == [(y, x) for y in range(3) for x in range(5)]
+
+
+def test_attention_rows_is_the_definition_on_the_selected_rows_and_heads():
+    # The large GPU tests evaluate the reference on sampled rows (and heads) only;
+    # each selected output must equal the pure-Python brute force of that row and head.
+    rng = np.random.default_rng(17)
+    q = rng.standard_normal((9, 3, 8))
+    k = rng.standard_normal((13, 3, 8))
+    v = rng.standard_normal((13, 3, 8))
+    rows, heads = np.array([0, 4, 8]), np.array([2, 0])
+    got = fo.attention_rows_f64(q, k, v, rows, heads)
+    assert got.shape == (3, 2, 8)
+    for a, r in enumerate(rows):
+        for b, hh in enumerate(heads):
+            bf = fo.attention_bruteforce([[q[r, hh].tolist()]], [[x.tolist()] for x in k[:, hh]],
+                                         [[x.tolist()] for x in v[:, hh]])
+            np.testing.assert_allclose(got[a, b], bf[0][0], rtol=0, atol=1e-12)
+    # all heads by default
+    assert fo.attention_rows_f64(q, k, v, rows).shape == (3, 3, 8)
+
+
+def test_published_k_is_the_rounded_exact_rotation():
+    # Published K = RoPE(K) rounded once to bf16.  Against exact rational arithmetic on
+    # the same fp64 cos/sin values (Python's math library, as the contract fixes), each
+    # element must be within one bf16 unit in the last place of the exact rotation: a
+    # dropped term, a flipped sign or a wrong pairing would be off by far more.
+    from fractions import Fraction
+    d = 64
+    rng = np.random.default_rng(23)
+    k = fo.f64_to_bf16_bits(rng.standard_normal((3, 2, d)))
+    pos = np.array([[3, 2, 5], [40, 29, 51], [0, 7, 0]], dtype=np.int64)
+    got = fo.bf16_bits_to_f64(fo.rope_k_bits(k, pos, d, 10000.0))
+    kf = fo.bf16_bits_to_f64(k)
+    dt, dy, dx = d - 4 * (d // 6), 2 * (d // 6), 2 * (d // 6)
+    axes = [(0, j, dt) for j in range(dt // 2)] + [(1, j, dy) for j in range(dy // 2)] + \
+           [(2, j, dx) for j in range(dx // 2)]
+    for n in range(3):
+        for h in range(2):
+            for p, (axis, j, da) in enumerate(axes):
+                ang = float(pos[n, axis]) * (10000.0 ** (-(2 * j) / da))
+                c, s = Fraction(math.cos(ang)), Fraction(math.sin(ang))
+                a, b = Fraction(kf[n, h, 2 * p]), Fraction(kf[n, h, 2 * p + 1])
+                for val, exact in ((got[n, h, 2 * p], a * c - b * s), (got[n, h, 2 * p + 1], a * s + b * c)):
+                    e = float(exact)
+                    ulp = 2.0 ** (math.frexp(e)[1] - 8) if e != 0 else 2.0 ** -133
+                    assert abs(val - e) <= ulp, (n, h, p, val, e)
