@@ -7,7 +7,9 @@ fp64 oracle:
     block by block just before the first chunk that needs them, with published
     K/V bytes and slot tags checked bit-exactly after every call;
   * every planner block of a second bank;
-  * the packed block-causal forward of one stage.
+  * the packed block-causal forward of one stage;
+  * the render schedule of a bank with 1-4 stages issued as stage-wavefront
+    batches (ff_render_attn_batch).
 The draws cover tokens-per-frame down to 1, short final chunks, anchors inside
 chunks, anchor-ring wrap-around and both head sizes, i.e. the segment layouts
 the attention kernel reads in place.
@@ -133,5 +135,52 @@ def test_random_description_planner_and_packed(ff, seed):
     torch.cuda.synchronize()
     mae, rl2, ok = compare_out(out, ref)
     assert ok, (f, "packed", mae, rl2)
+    assert bank.error_poll() == 0
+    bank.close()
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_random_description_wavefront_batches(ff, seed):
+    """The render schedule of a drawn description with 1-4 stages issued as
+    stage-wavefront batches (ff_render_attn_batch: at step w, stage k renders
+    chunk w - k), every anchor resident; each call against the oracle, slot
+    bytes after every batch."""
+    from kv_cache_attention_ff_gb300 import synth
+    r = np.random.default_rng(3000 + seed)
+    f = _draw(seed)
+    N, B, S = f["total_frames"], f["chunk_frames"], f["anchor_stride"]
+    f = dict(f, n_stages=int(r.integers(1, 5)), anchor_capacity=fo.num_anchors(N, S))
+    cfg_id = 400 + seed
+    dev = torch.device("cuda:0")
+    T, h, d = f["frame_h"] * f["frame_w"], f["heads"], f["head_dim"]
+    bank = ff.Bank(**f)
+    obank = fo.OracleBank(oracle_cfg(f))
+    anchors = list(range(0, N, S))
+    kb = synth.frames_tensor(cfg_id, 0, synth.ANCHOR_STREAM, synth.K, anchors, T, h, d, "normal")
+    vb = synth.frames_tensor(cfg_id, 0, synth.ANCHOR_STREAM, synth.V, anchors, T, h, d, "normal")
+    for j in range(0, len(anchors), 3):
+        n = min(3, len(anchors) - j)
+        sl = slice(j * T, (j + n) * T)
+        bank.anchor_publish(0, anchors[j], n, from_bits(kb[sl], dev), from_bits(vb[sl], dev))
+        obank.anchor_publish(0, anchors[j], n, kb[sl], vb[sl])
+    nc, ns = fo.num_chunks(N, B), f["n_stages"]
+    for w in range(nc + ns - 1):
+        calls, refs = [], []
+        for st in range(ns):
+            i = w - st
+            if not 0 <= i < nc:
+                continue
+            s, e = fo.chunk_span(i, B, N)
+            frames = list(range(s, e + 1))
+            q, k, v = (synth.frames_tensor(cfg_id, 0, st, t, frames, T, h, d, "normal") for t in range(3))
+            out = torch.full((len(frames) * T, h, d), float("nan"), dtype=torch.bfloat16, device=dev)
+            calls.append((0, st, i, from_bits(q, dev), from_bits(k, dev), from_bits(v, dev), out))
+            refs.append(obank.render(0, st, i, q, k, v).out)
+        bank.render_attn_batch(calls)
+        torch.cuda.synchronize()
+        for c, ref in zip(calls, refs):
+            mae, rl2, ok = compare_out(c[6], ref)
+            assert ok, (f, w, c[1], c[2], mae, rl2)
+            _check_slots(bank, obank, c[1])
     assert bank.error_poll() == 0
     bank.close()
