@@ -487,13 +487,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // Merge the key-range pieces of each (head, query block): with per-piece
 // running max m_s (log2 units), sum l_s and unnormalised O_s,
 //   m = max m_s,  l = sum l_s 2^(m_s - m),  O = sum O_s 2^(m_s - m) / l.
-// One thread per 8 output columns of a row; it issues the loads of all pieces
-// before the first use, so the merge costs one round trip to L2.
+// One thread per 16 output columns of a row; it issues the loads of all pieces
+// before the first use, so the merge costs one round trip to L2, and a split
+// unit's 256 rows take 256 / (128 / (d / 16)) blocks: one wave of 8 blocks per
+// SM for the 76 split units of a 1.3B call.
 constexpr int kCombineThreads = 128;
+constexpr int kCombinePer = 16;  // output columns per thread
 
-template <int D, class P>
-__global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const __grid_constant__ P p) {
-  constexpr int PER = 8;                           // columns per thread
+template <int D, int NS, class P>
+__global__ void __launch_bounds__(kCombineThreads, NS == 2 ? 8 : 4) attn_combine_kernel(const __grid_constant__ P p) {
+  constexpr int PER = kCombinePer;
   constexpr int TPR = D / PER;                     // threads per row
   constexpr int ROWS = kCombineThreads / TPR;      // rows per block
   const int rest = p.heads * p.n_qb - p.n_whole;  // split units
@@ -510,13 +513,12 @@ __global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const 
   const int lrow = qb * 256 + rloc;
   if (lrow >= G.nq) return;
   const int row = G.out_row0 + lrow;
-  const int ns = p.n_split;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  float2 mls[kMaxSplit];
-  float4 os[kMaxSplit][PER / 4];
+  float2 mls[NS];
+  float4 os[NS][PER / 4];
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < ns) {
+  for (int s = 0; s < NS; ++s) {
+    {
       const size_t piece = static_cast<size_t>(s) * rest + ru;
       mls[s] = ml[piece * 256 + rloc];
       const float4* src = reinterpret_cast<const float4*>(p.part_o + (piece * 256 + rloc) * D + part * PER);
@@ -526,15 +528,14 @@ __global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const 
   }
   float m = -INFINITY;
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s)
-    if (s < ns) m = fmaxf(m, mls[s].x);
+  for (int s = 0; s < NS; ++s) m = fmaxf(m, mls[s].x);
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float l = 0.f;
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < ns) {
+  for (int s = 0; s < NS; ++s) {
+    {
       const float w = exp2f(mls[s].x - m);
       l = __fmaf_rn(mls[s].y, w, l);
 #pragma unroll
@@ -551,7 +552,9 @@ __global__ void __launch_bounds__(kCombineThreads, 8) attn_combine_kernel(const 
   uint32_t w[PER / 2];
 #pragma unroll
   for (int i = 0; i < PER / 2; ++i) w[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+  for (int i = 0; i < PER / 8; ++i)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 size_t attention_smem_bytes(int head_dim) {
@@ -590,12 +593,22 @@ void launch_attn_p(int head_dim, const CUtensorMap& tq, const KV& kv, const P& p
     bank_attn_kernel<64><<<grid, kAttnThreads, AttnCfg<64>::SMEM, s>>>(tq, kv, p);
 }
 
+template <int NS, class P>
+void launch_combine_ns(int head_dim, const P& p, dim3 grid, cudaStream_t s) {
+  if (head_dim == 128)
+    attn_combine_kernel<128, NS><<<grid, kCombineThreads, 0, s>>>(p);
+  else
+    attn_combine_kernel<64, NS><<<grid, kCombineThreads, 0, s>>>(p);
+}
+
 template <class P>
 void launch_combine_p(int head_dim, const P& p, dim3 grid, cudaStream_t s) {
-  if (head_dim == 128)
-    attn_combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p);
+  if (p.n_split == 2)
+    launch_combine_ns<2>(head_dim, p, grid, s);
+  else if (p.n_split == 3)
+    launch_combine_ns<3>(head_dim, p, grid, s);
   else
-    attn_combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p);
+    launch_combine_ns<kMaxSplit>(head_dim, p, grid, s);
 }
 }  // namespace
 
@@ -620,8 +633,8 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tq, const KVMapsBa
 }
 
 cudaError_t launch_combine(int head_dim, const AttnParams& p, cudaStream_t s) {
-  // split units x 256 rows in blocks of 128 / (d / 8) rows
-  dim3 grid(p.heads * p.n_qb - p.n_whole, 256 / (kCombineThreads / (head_dim / 8)));
+  // split units x 256 rows in blocks of 128 / (d / 16) rows
+  dim3 grid(p.heads * p.n_qb - p.n_whole, 256 / (kCombineThreads / (head_dim / kCombinePer)));
   if (p.n_groups == 1)
     launch_combine_p(head_dim, first_groups<1>(p), grid, s);
   else if (p.n_groups <= kMaxBatch)
