@@ -43,9 +43,13 @@ Readings where the pages are silent (each is also listed in the design notes):
 
 Parity status: every function below is pinned by tests under
 ``tests/test_oracle_*.py`` against closed forms, library routines, worked
-tables or brute force, except the RoPE *layout* (which axis gets which
-channels), which is "parity unpinned" with respect to the pages because the
-pages never print it; its internal consistency is pinned.
+tables, exact rational arithmetic or brute force.  What no test can tie to the
+pages is the RoPE *layout* choice itself (which axis gets which channels): the
+pages name RoPE but never print a layout, so the layout is a reading
+("parity unpinned" with respect to the pages), while the functions that
+implement it are pinned (identity at the origin, textbook values, axis and
+frequency mapping, pair norms, the relative-position identity, the rounded
+exact rotation).
 """
 from __future__ import annotations
 
