@@ -117,3 +117,40 @@ def test_planner_plan_matches_oracle(ff, fields):
         assert p.key_frames == len(own) + B * len(hist)
     with pytest.raises(ff.FFError):
         ff.plan_planner_block(d, nb)
+
+
+def test_entry_points_reject_a_null_bank(ff):
+    # Every entry point that takes a bank returns FF_ERR_ARG for a null one, on the
+    # host, before any device work (no GPU needed).
+    lib = ff.lib()
+    null = ctypes.c_void_p()
+    p = ctypes.c_void_p(16)  # never dereferenced: the bank check comes first
+    assert lib.ff_anchor_publish(null, 0, 0, 1, p, p, None) == 1
+    assert lib.ff_render_attn(null, 0, 0, 0, p, p, p, p, None) == 1
+    calls = (ff.RenderCall * 2)()
+    assert lib.ff_render_attn_batch(null, 2, calls, None) == 1
+    assert lib.ff_planner_attn(null, 0, 0, p, p, p, p, None) == 1
+    n = ctypes.c_size_t()
+    assert lib.ff_packed_workspace_bytes(null, ctypes.byref(n)) == 1
+    assert lib.ff_bank_bytes(null, ctypes.byref(n)) == 1
+    assert lib.ff_bank_error_poll(null) == 1
+    assert lib.ff_bank_set_timing(null, 1) == 1
+    t = ff.KernelTimes()
+    assert lib.ff_bank_read_timing(null, ctypes.byref(t)) == 1
+    c = ctypes.c_int()
+    assert lib.ff_render_kernel_count(null, 0, ctypes.byref(c)) == 1
+    assert lib.ff_bank_wait_probe(null, 10, None) == 1
+    assert lib.ff_bank_destroy(null) == 0
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host(ff):
+    # Null pointers, unsupported head sizes, misaligned pointers and sizes past the
+    # index limits are refused before the library touches a device.
+    lib = ff.lib()
+    p = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(258)
+    assert lib.ff_attention_noalloc(None, p, p, p, 16, 16, 1, 64, None) == 1
+    assert lib.ff_attention_noalloc(p, p, p, p, 16, 16, 1, 96, None) == 1
+    assert lib.ff_attention_noalloc(p, odd, p, p, 16, 16, 1, 64, None) == 1
+    assert lib.ff_attention_noalloc(p, p, p, p, 16, 1 << 25, 1, 64, None) == 1
+    assert lib.ff_attention_noalloc(p, p, p, p, 0, 16, 1, 64, None) == 1
