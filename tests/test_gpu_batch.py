@@ -169,3 +169,54 @@ def test_wan13b_480p_four_stage_batch_sampled(ff):
             assert tag == i and np.array_equal(to_bits(sk), k_rot) and np.array_equal(to_bits(sv), vb), (st, i)
     assert bank.error_poll() == 0
     bank.close()
+
+
+def test_wan14b_480p_four_stage_batch_sampled_heads(ff):
+    """The 14B 480p shape (40 heads, 4680 queries over 31200 keys) at all four stages
+    in one batch (chunk 5 of each stage after batches of chunks 0..4): slot bytes
+    bit-exact on 3 heads at every chunk, sampled rows of 3 heads of every call
+    against the oracle's definition on those heads."""
+    from kv_cache_attention_ff_gb300 import synth
+    cfg_id, fields, mode = CONFIGS["wan14b_480p"]
+    T, h, d = 1560, fields["heads"], fields["head_dim"]
+    dev = torch.device("cuda:0")
+    heads = np.array([0, 21, 39])
+    bank = ff.Bank(**fields)
+    ka = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.K, [0, 10, 20], T, h, d, mode)
+    va = synth.device_frames(cfg_id, 0, synth.ANCHOR_STREAM, synth.V, [0, 10, 20], T, h, d, "normal")
+    bank.anchor_publish(0, 0, 3, ka, va)
+    anc_k = {a: fo.rope_k_bits(to_bits(ka[j * T:(j + 1) * T])[:, heads], fo.token_positions([a], 30, 52), d, 1e4)
+             for j, a in enumerate((0, 10, 20))}
+    anc_v = {a: to_bits(va[j * T:(j + 1) * T])[:, heads] for j, a in enumerate((0, 10, 20))}
+    streams = {st: [synth.DeviceARStream(cfg_id, 0, st, t, T, h, d, mode if t < 2 else "normal")
+                    for t in (synth.Q, synth.K, synth.V)] for st in range(4)}
+    hist = {st: {} for st in range(4)}   # chunk -> (rotated K bits, V bits) of the checked heads
+    rng = np.random.default_rng(13)
+    rows = np.unique(np.concatenate([[0, 255, 256, 4607, 4608, 4679], rng.choice(4680, 26, replace=False)]))
+    outs = [torch.empty((3 * T, h, d), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    for i in range(6):
+        s, e = fo.chunk_span(i, 3, 81)
+        pos = fo.token_positions(list(range(s, e + 1)), 30, 52)
+        inputs = [[x.frames(3) for x in streams[st]] for st in range(4)]
+        bank.render_attn_batch([(0, st, i, *inputs[st], outs[st]) for st in range(4)])
+        torch.cuda.synchronize()
+        for st in range(4):
+            q, k, v = (to_bits(x)[:, heads] for x in inputs[st])
+            k_rot = fo.rope_k_bits(k, pos, d, 1e4)
+            hist[st][i] = (k_rot, v)
+            tag, sk, sv = bank.slot_tensors(0, st, i % 5)
+            assert tag == i
+            assert np.array_equal(to_bits(sk)[:, heads], k_rot) and np.array_equal(to_bits(sv)[:, heads], v), (st, i)
+            if i == 5:
+                ks = [anc_k[a] for a in (10, 20)] + [hist[st][j][0] for j in range(0, 6)]
+                vs = [anc_v[a] for a in (10, 20)] + [hist[st][j][1] for j in range(0, 6)]
+                K = fo.bf16_bits_to_f64(np.concatenate(ks))
+                V = fo.bf16_bits_to_f64(np.concatenate(vs))
+                assert K.shape[0] == 20 * T
+                Q = fo.rope_q_f64(q, pos, d, 1e4)
+                ref = fo.attention_rows_f64(Q, K, V, rows)
+                got = outs[st][torch.from_numpy(rows).to(dev)][:, torch.from_numpy(heads).to(dev)]
+                mae, rl2, ok = compare_out(got, ref)
+                assert ok, (st, mae, rl2)
+    assert bank.error_poll() == 0
+    bank.close()
