@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # source digest the counters belong to and the calls the captured launch covered: a
 # kernel edited since then, or a launch of another size, reports null.
 NCU_TRAFFIC = {
-    "bank_attn_kernel": (838.6e6, "ff_attn.cu", "823e09e96ddf20cf", 4),
+    "bank_attn_kernel": (838.6e6, "ff_attn.cu", "961f0ca6a71ba0a2", 4),
     "rope_publish_kernel": (288.6e6, "ff_publish.cu", "f39c3097d7c98795", 4),
 }
 

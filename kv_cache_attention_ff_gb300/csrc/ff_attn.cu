@@ -23,12 +23,15 @@
 // final normalisation uses the same stale max, which keeps the result exact
 // up to rounding.
 //
-// Work split: a (head, query block) unit covers n_kv key tiles.  The first
-// n_whole units run as one piece each; the rest are cut into n_split key
-// ranges, so that the persistent CTAs (taking pieces round-robin) finish
-// together.  Units are ordered (head, query block), split pieces (split, unit),
-// so concurrently running CTAs stream the same key tiles (L2 reuse).  Split
-// pieces write unnormalised partials that a small combine kernel merges.
+// Work split: a launch carries one or more query groups (a renderer call,
+// each call of a stage-wavefront batch, each chunk of a packed forward), each
+// with its own key segments and output.  A (head, query block) unit covers its
+// group's n_kv key tiles.  The first n_whole units run as one piece each; the
+// rest are cut into n_split key ranges, so that the persistent CTAs (taking
+// pieces round-robin) finish together.  Units are ordered (head, query block),
+// split pieces (split, unit), so concurrently running CTAs stream the same key
+// tiles (L2 reuse).  Split pieces write unnormalised partials that a small
+// combine kernel merges.
 #include <cuda_bf16.h>
 
 #include "ff_internal.h"
