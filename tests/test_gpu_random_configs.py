@@ -12,7 +12,8 @@ fp64 oracle:
     batches (ff_render_attn_batch).
 The draws cover tokens-per-frame down to 1, short final chunks, anchors inside
 chunks, anchor-ring wrap-around and both head sizes, i.e. the segment layouts
-the attention kernel reads in place.
+the attention kernel reads in place; six larger draws (frames of 20-400 tokens,
+up to 8 heads) give segments of many key tiles and split work plans.
 """
 import numpy as np
 import pytest
@@ -24,6 +25,8 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 SEEDS = list(range(12))
+# larger draws (frames of 20-400 tokens, up to 8 heads: segments of many key tiles)
+BIG = [100 + s for s in range(6)]
 
 
 @pytest.fixture(scope="module")
@@ -36,6 +39,8 @@ def ff():
 
 
 def _draw(seed):
+    if seed >= 100:
+        return _draw_big(seed - 100)
     r = np.random.default_rng(1000 + seed)
     B = int(r.integers(1, 5))
     stride = int(r.integers(1, 7))
@@ -50,6 +55,19 @@ def _draw(seed):
                 head_dim=int(r.choice([64, 128])), frame_h=int(r.integers(1, 6)), frame_w=int(r.integers(1, 8)))
 
 
+def _draw_big(seed):
+    r = np.random.default_rng(5000 + seed)
+    B = int(r.integers(1, 5))
+    stride = int(r.integers(2, 9))
+    N = int(r.integers(8, 30))
+    A = fo.num_anchors(N, stride)
+    need = 3 * (-(-B // stride) + 3)
+    cap = A if r.random() < 0.5 else min(A, max(need, 6))
+    return dict(n_layers=1, n_stages=int(r.integers(1, 3)), history=int(r.integers(1, 6)), chunk_frames=B,
+                anchor_stride=stride, anchor_capacity=cap, total_frames=N, heads=int(r.integers(1, 9)),
+                head_dim=int(r.choice([64, 128])), frame_h=int(r.integers(4, 21)), frame_w=int(r.integers(5, 21)))
+
+
 def _check_slots(bank, obank, stage):
     for s in range(obank.cfg.history):
         tag, k, v = bank.slot_tensors(0, stage, s)
@@ -59,7 +77,7 @@ def _check_slots(bank, obank, stage):
             assert np.array_equal(to_bits(k), osl.k) and np.array_equal(to_bits(v), osl.v)
 
 
-@pytest.mark.parametrize("seed", SEEDS)
+@pytest.mark.parametrize("seed", SEEDS + BIG)
 def test_random_description_render_schedule(ff, seed):
     from kv_cache_attention_ff_gb300 import synth
     f = _draw(seed)
@@ -96,7 +114,7 @@ def test_random_description_render_schedule(ff, seed):
     bank.close()
 
 
-@pytest.mark.parametrize("seed", SEEDS)
+@pytest.mark.parametrize("seed", SEEDS + BIG)
 def test_random_description_planner_and_packed(ff, seed):
     from kv_cache_attention_ff_gb300 import synth
     f = _draw(seed)
@@ -139,7 +157,7 @@ def test_random_description_planner_and_packed(ff, seed):
     bank.close()
 
 
-@pytest.mark.parametrize("seed", SEEDS)
+@pytest.mark.parametrize("seed", SEEDS + BIG)
 def test_random_description_wavefront_batches(ff, seed):
     """The render schedule of a drawn description with 1-4 stages issued as
     stage-wavefront batches (ff_render_attn_batch: at step w, stage k renders
