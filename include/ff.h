@@ -253,7 +253,11 @@ typedef struct ff_kernel_times {
 } ff_kernel_times;
 
 /* enable != 0: record events around each kernel launch of subsequent renderer
- * calls (ff_render_attn, ff_render_attn_batch).  Resets the accumulated times. */
+ * calls (ff_render_attn, ff_render_attn_batch).  Resets the accumulated times.
+ * Synchronises the bank's device; the events are created here (2048 calls'
+ * worth, and that many more whenever a run of timed calls without a reset
+ * needs them), so timed calls record into existing events.  Returns
+ * FF_ERR_CUDA if the events cannot be created. */
 int ff_bank_set_timing(ff_bank_t* bank, int enable);
 
 /* Synchronise on the recorded events and return the accumulated times. */
